@@ -1,0 +1,537 @@
+"""Benchmark: MoE dispatch + combine on one GB300 (R ranks emulated in HBM).
+
+One step = one pass of the hot path over one batch:
+  decode (default, low-latency): ep_ll_dispatch (layout + FP8 ue8m0
+      scatter into the packed masked layout) + ep_ll_combine;
+  prefill / large / skewed (normal mode): ep_get_dispatch_layout +
+      ep_notify_dispatch (+ the host handshake unless num_worst_tokens) +
+      ep_dispatch + ep_combine.
+Inputs are resident in HBM before the timed region; L2 is flushed (512 MiB
+write) before every step, outside the per-step CUDA events.  The JSON line
+reports the decode workload; the other workloads are measured in the same
+run under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workloads decode,prefill,skewed,large]
+
+With N > 1 (torchrun) every rank runs an independent replica (the emulated
+ranks live inside one GPU; there is no data-path collective): weak scaling,
+value = total tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+HEADLINE = "decode"
+FLUSH_BYTES = 512 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workloads", default="decode,prefill,skewed,large")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_init(n_gpus: int):
+    """(rank, world, local_rank); torch.distributed only when launched by torchrun."""
+    if "RANK" in os.environ and "WORLD_SIZE" in os.environ and int(os.environ["WORLD_SIZE"]) > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("EP_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+        return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", 0))
+    return 0, 1, 0
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workloads
+
+def alg_bytes(w, rows: int):
+    """Algorithmic bytes: dispatch reads each source row once and writes one
+    row per routed slot (bf16, or E4M3 + scales); combine reads one bf16 row
+    per routed slot and writes one bf16 row per token."""
+    row_in = 2 * w.H
+    if w.fp8_mode == 0:
+        row_out = 2 * w.H
+    else:
+        row_out = w.H + (w.H // 128) * (4 if w.fp8_mode == 1 else 1)
+    dispatch = w.T * row_in + rows * row_out
+    combine = rows * 2 * w.H + w.T * 2 * w.H
+    return dispatch, combine
+
+
+class Runner:
+    """Buffers and one step of one workload on the current GPU."""
+
+    def __init__(self, w, device):
+        import numpy as np
+        import torch
+
+        from combine_get_dispatch_gb300 import ep, synth
+        self.w, self.dev, self.ep = w, device, ep
+        idx, wts = synth.routing(w)
+        self.idx = torch.from_numpy(idx).to(device)
+        self.wts = torch.from_numpy(wts).to(device)
+        self.x = synth.activations_torch(w, device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, device=device)
+        self.out = torch.empty_like(self.x)
+        self.rows = int((idx >= 0).sum())
+        self.ll = w.mode == "ll"
+        if self.ll:
+            self.buf = ep.alloc_ll(w.R, w.T_r, w.H, w.E, w.k, w.max_tokens_per_rank, w.fp8_mode,
+                                   device=device)
+            S = w.R * w.max_tokens_per_rank
+            self.y = synth.expert_outputs_torch(w.E * S, w.H, device).view(w.R, w.E_l, S, w.H)
+        else:
+            self.lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E, device=device)
+            self.nt = ep.alloc_notify(w.R, w.E, device=device)
+            self.host_rows = torch.empty(w.R, dtype=torch.int64).pin_memory()
+            if w.num_worst_tokens >= 0:
+                self.cap = w.cap_rows()
+            else:   # size the receive buffers from one handshake (as the caller would)
+                self._layout_notify()
+                self.cap = int(self.host_rows.max())
+            self.buf = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, self.cap, device=device)
+            self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(w.R, self.cap, w.H)
+        torch.cuda.synchronize()
+
+    def _layout_notify(self):
+        ep, w = self.ep, self.w
+        ep.ep_get_dispatch_layout(self.idx, w.E, self.lay["num_tokens_per_rank"],
+                                  self.lay["num_tokens_per_expert"], self.lay["is_token_in_rank"],
+                                  self.lay["slot_rank"], self.ws, self.status)
+        ep.ep_notify_dispatch(self.lay["num_tokens_per_rank"], self.lay["num_tokens_per_expert"],
+                              w.expert_alignment, w.num_worst_tokens,
+                              self.nt["rank_prefix_matrix"], self.nt["expert_prefix"],
+                              self.nt["num_recv_tokens_per_expert"], self.nt["psum"],
+                              self.host_rows if w.num_worst_tokens < 0 else None, 10000,
+                              self.status)
+
+    def step(self, ev=None):
+        """One pass; ev = (e0, e1, e2, e3) events around dispatch / combine."""
+        ep, w, b = self.ep, self.w, self.buf
+        if self.ll:
+            if ev:
+                ev[0].record()
+            ep.ep_ll_dispatch(self.x, self.idx, w.E, w.max_tokens_per_rank, w.fp8_mode,
+                              b["packed_recv_x"], b["packed_recv_scales"],
+                              b["packed_recv_src_info"], b["layout_range"], b["recv_count"],
+                              b["combine_idx"], self.ws, self.status)
+            if ev:
+                ev[1].record()
+                ev[2].record()
+            ep.ep_ll_combine(self.y, self.wts, b["combine_idx"], w.E, w.max_tokens_per_rank,
+                             self.out, self.status)
+            if ev:
+                ev[3].record()
+        else:
+            self._layout_notify()
+            if ev:
+                ev[0].record()
+            ep.ep_dispatch(self.x, self.idx, self.lay["slot_rank"], self.nt["expert_prefix"],
+                           self.nt["psum"], w.E, w.fp8_mode, self.cap, b["recv_x"],
+                           b["recv_scales"], b["recv_src_idx"], b["combine_idx"], self.status)
+            if ev:
+                ev[1].record()
+                ev[2].record()
+            ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
+            if ev:
+                ev[3].record()
+
+
+def workload_desc(w) -> str:
+    fp8 = {0: "bf16", 1: "FP8 E4M3 + fp32 per-128 scales", 2: "FP8 E4M3 + ue8m0 per-128 scales"}
+    mode = "low-latency packed" if w.mode == "ll" else "normal contiguous"
+    extra = f", num_worst_tokens={w.num_worst_tokens}" if w.num_worst_tokens >= 0 else ""
+    return (f"{w.name}: R={w.R} x {w.T_r} tokens/rank, H={w.H}, E={w.E} ({w.E_l}/rank), "
+            f"top-{w.k}, {fp8[w.fp8_mode]} {mode} dispatch + bf16 combine{extra}")
+
+
+def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
+    import torch
+
+    ep = runner.ep
+    for _ in range(warmup):
+        flush.fill_(1)
+        runner.step()
+    torch.cuda.synchronize()
+    code = ep.ep_read_status(runner.status)
+    if code != ep.EP_OK:
+        raise RuntimeError(f"{runner.w.name}: kernel status {ep.error_string(code)}")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    barrier(world, runner.dev)
+    torch.cuda.synchronize()
+    launches0 = ep.ep_launch_count()
+    t_wall = time.perf_counter()
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        e = evs[s]
+        e[4].record()
+        runner.step(e[:4])
+        e[5].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    barrier(world, runner.dev)
+    launches = ep.ep_launch_count() - launches0
+    step_ms = [e[4].elapsed_time(e[5]) for e in evs]
+    disp_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    res = {"step_ms": statistics.mean(step_ms), "step_ms_min": min(step_ms),
+           "dispatch_ms": statistics.mean(disp_ms), "combine_ms": statistics.mean(comb_ms),
+           "launches": launches, "wall_s": wall}
+    if e2e:
+        res["e2e"] = measure_e2e(runner, steps, world, flush)
+    return res
+
+
+def measure_e2e(runner, steps, world, flush):
+    """Same step through the public API with the inputs copied from pinned
+    host memory and the output read back, inside the timed region."""
+    import torch
+
+    hx = runner.x.cpu().pin_memory()
+    hi = runner.idx.cpu().pin_memory()
+    hw = runner.wts.cpu().pin_memory()
+    ho = torch.empty(runner.out.shape, dtype=runner.out.dtype).pin_memory()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    barrier(world, runner.dev)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        evs[s][0].record()
+        runner.x.copy_(hx, non_blocking=True)
+        runner.idx.copy_(hi, non_blocking=True)
+        runner.wts.copy_(hw, non_blocking=True)
+        runner.step()
+        ho.copy_(runner.out, non_blocking=True)
+        evs[s][1].record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    h2d = hx.numel() * hx.element_size() + hi.numel() * 8 + hw.numel() * 4
+    d2h = ho.numel() * ho.element_size()
+    return {"ms": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def kernel_hash(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(kernel: str, workload: str, src: str):
+    """dram bytes per launch from the committed ncu summary, if it still
+    matches the kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d[f"{kernel}:{workload}"]
+        if ent.get("source_sha") == kernel_hash(src):
+            return ent["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_step(w, x_bits, idx, wts, y_rows, tokens_per_rank: int):
+    """The oracle's dispatch + combine on the first tokens_per_rank tokens of
+    every rank (a bounded sample of the workload).  Returns tokens done."""
+    import numpy as np
+
+    import oracle
+    xs = np.ascontiguousarray(x_bits[:, :tokens_per_rank])
+    ids = np.ascontiguousarray(idx[:, :tokens_per_rank])
+    ws = np.ascontiguousarray(wts[:, :tokens_per_rank])
+    if w.mode == "ll":
+        d = oracle.ll_dispatch(xs, ids, w.E, w.max_tokens_per_rank, w.fp8_mode, fill=None)
+    else:
+        lay = oracle.layout(ids, w.R, w.E)
+        nt = oracle.notify(lay["num_tokens_per_rank"], lay["num_tokens_per_expert"], w.R, w.E,
+                           w.expert_alignment)
+        cap = max(1, int(nt["psum"][:, -1].max()))
+        d = oracle.dispatch(xs, ids, lay["slot_rank"], nt["expert_prefix"], nt["psum"], w.E,
+                            w.fp8_mode, cap, fill=None)
+    cidx = d["combine_idx"]
+    # expert outputs for the rows this sample routes to (stand-in values)
+    m = cidx >= 0
+    remap = np.full(cidx.shape, -1, np.int32)
+    remap[m] = np.arange(int(m.sum()), dtype=np.int32)
+    oracle.combine(y_rows[: int(m.sum())], ws, remap, w.H)
+    return w.R * tokens_per_rank
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    import numpy as np
+
+    import oracle
+    from combine_get_dispatch_gb300 import synth
+    oracle.build()
+    idx, wts = synth.routing(w)
+    tpr = max(1, w.T_r // 8) if w.T_r >= 8 else w.T_r
+    sub = synth.scaled(w, T_r=tpr)
+    x_bits = synth.activations(sub)
+    y_rows = synth.expert_outputs(w.R * tpr * w.k, w.H)
+    done, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        done += oracle_step(w, x_bits, idx, wts, y_rows, tpr)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s or reps >= 8:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{reps} x oracle dispatch+combine of the first {tpr} tokens of each of "
+                       f"the {w.R} ranks ({w.R * tpr} tokens, 1/{w.T_r // tpr} of the workload), "
+                       f"single-threaded C, {el:.1f} s")}
+
+
+# ---------------------------------------------------------------- main
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from combine_get_dispatch_gb300 import synth
+    w = synth.WORKLOADS[HEADLINE]
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    idx, wts = synth.routing(w)
+    tpr = max(1, w.T_r // 8)
+    sub = synth.scaled(w, T_r=tpr)
+    x_bits = synth.activations(sub)
+    y_rows = synth.expert_outputs(w.R * tpr * w.k, w.H)
+    for _ in range(args.warmup):
+        oracle_step(w, x_bits, idx, wts, y_rows, tpr)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        n = oracle_step(w, x_bits, idx, wts, y_rows, tpr)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = n / (ms / 1e3)
+    sample = (f"oracle (single-threaded C) dispatch+combine of the first {tpr} tokens of each "
+              f"of the {w.R} ranks per step ({n} tokens)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": workload_desc(w)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from combine_get_dispatch_gb300 import ep, synth
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ep.load()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak, peak_kind = peaks()
+    names = [n.strip() for n in args.workloads.split(",") if n.strip()]
+    if HEADLINE not in names:
+        names.insert(0, HEADLINE)
+    results = {}
+    clocks = None
+    for name in names:
+        w = synth.WORKLOADS[name]
+        runner = Runner(w, dev)
+        sampler = ClockSampler(local_rank) if name == HEADLINE else None
+        if sampler:
+            sampler.start()
+        res = measure(runner, args.steps, args.warmup, world, flush,
+                      e2e=(name == HEADLINE and not args.no_e2e))
+        if sampler:
+            clocks = sampler.stop()
+        res["step_ms_max"] = max_over_ranks(res["step_ms"], world)
+        dbytes, cbytes = alg_bytes(w, runner.rows)
+        res["dispatch_alg_bytes"], res["combine_alg_bytes"] = dbytes, cbytes
+        res["dispatch_gbs"] = dbytes / (res["dispatch_ms"] * 1e-3) / 1e9
+        res["combine_gbs"] = cbytes / (res["combine_ms"] * 1e-3) / 1e9
+        res["tokens"] = w.T
+        results[name] = (w, runner, res)
+        if name != HEADLINE:
+            del runner
+            torch.cuda.empty_cache()
+
+    w, runner, res = results[HEADLINE]
+    ms = res["step_ms_max"]
+    value = world * w.T / (ms * 1e-3)
+    e2e = None
+    if "e2e" in res:
+        e2e_ms = max_over_ranks(res["e2e"]["ms"], world)
+        e2e = {"value": world * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": res["e2e"]["h2d_bytes_per_step"],
+               "d2h_bytes_per_step": res["e2e"]["d2h_bytes_per_step"], "ms_per_step": e2e_ms}
+    # dominant kernel of the headline step: the one with the larger time
+    dom = "combine" if res["combine_ms"] >= res["dispatch_ms"] else "dispatch"
+    kern = {"combine": "k_combine", "dispatch": "k_scatter"}[dom]
+    src = os.path.join(ROOT, "combine_get_dispatch_gb300", "csrc",
+                       "combine.cu" if dom == "combine" else "dispatch.cu")
+    achieved = res[f"{dom}_gbs"]
+    roofline = {"bound": "hbm", "kernel": kern, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "alg_bytes_per_launch": res[f"{dom}_alg_bytes"],
+                "traffic": load_traffic(kern, HEADLINE, src)}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(w), "l2": "flushed before every step (512 MiB write)",
+                       "parallelism": f"{world} replica(s), {w.R} ranks emulated per GPU",
+                       "data_types": "x bf16 -> E4M3+ue8m0 dispatch; y bf16 -> bf16 combine, fp32 accumulate"},
+            "hbm_gbs": {"dispatch": round(res["dispatch_gbs"], 1),
+                        "combine": round(res["combine_gbs"], 1),
+                        "dispatch_frac": round(res["dispatch_gbs"] / peak, 4),
+                        "combine_frac": round(res["combine_gbs"] / peak, 4)},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": res["launches"],
+            "roofline": roofline}
+    others = {}
+    for name, (wo, _, r) in results.items():
+        if name == HEADLINE:
+            continue
+        others[name] = {
+            "workload": workload_desc(wo), "tokens_per_s": wo.T / (r["step_ms_max"] * 1e-3),
+            "ms_per_step": round(r["step_ms_max"], 4),
+            "dispatch_ms": round(r["dispatch_ms"], 4), "combine_ms": round(r["combine_ms"], 4),
+            "dispatch_gbs": round(r["dispatch_gbs"], 1), "combine_gbs": round(r["combine_gbs"], 1),
+            "dispatch_frac": round(r["dispatch_gbs"] / peak, 4),
+            "combine_frac": round(r["combine_gbs"] / peak, 4),
+            "layout_notify_ms": round(r["step_ms"] - r["dispatch_ms"] - r["combine_ms"], 4),
+            "gpu_launches": r["launches"]}
+    line["workloads"] = others
+    line["kernels_ms"] = {"dispatch": round(res["dispatch_ms"], 5),
+                          "combine": round(res["combine_ms"], 5)}
+    if rank == 0:
+        if world == 1:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_init(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,84 @@
+// api.cu -- host-side helpers and the small entry points of libep.
+
+#include <atomic>
+#include <mutex>
+
+#include "ep_common.cuh"
+
+namespace ep_host {
+
+static std::atomic<uint64_t> g_launches{0};
+
+int num_sms() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 1;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int check_launch() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+}  // namespace ep_host
+
+extern "C" int ep_clean_ll_buffer(int32_t* recv_count, int R, int E, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (R <= 0 || E <= 0 || E % R != 0) return EP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (recv_count != nullptr &&
+      cudaMemsetAsync(recv_count, 0, sizeof(int32_t) * (size_t)E, s) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
+  if (workspace != nullptr && workspace_bytes > 0 &&
+      cudaMemsetAsync(workspace, 0, workspace_bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
+  return EP_OK;
+}
+
+extern "C" int ep_read_status(const int32_t* status, int32_t* host_value, void* stream) {
+  if (status == nullptr || host_value == nullptr) return EP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_value, status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
+  return EP_OK;
+}
+
+extern "C" uint64_t ep_launch_count(void) {
+  return ep_host::g_launches.load(std::memory_order_relaxed);
+}
+
+extern "C" const char* ep_error_string(int code) {
+  switch (code) {
+    case EP_OK: return "ok";
+    case EP_ERR_INVALID_ARG: return "invalid argument";
+    case EP_ERR_CAPACITY: return "receive buffer capacity exceeded";
+    case EP_ERR_TIMEOUT: return "wait timed out";
+    case EP_ERR_CUDA: return "CUDA error";
+    case EP_ERR_STATE: return "workspace not initialised (call ep_clean_ll_buffer)";
+    default: return "unknown error";
+  }
+}

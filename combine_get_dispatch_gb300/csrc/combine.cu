@@ -1,0 +1,176 @@
+// combine.cu -- top-k weighted combine back to token order (llm-infra-atlas
+// DeepEP article §1.1 "FP8 dispatch, BF16 combine", §2.3 / §4.3: combine
+// walks the dispatch handle backwards).
+//
+//   out[t][:] = bf16_rn( fp32 fma chain over j = 0..k-1 of w[t][j] * y[f_j][:] )
+//
+// with f_j = combine_idx[t][j] (flat receive row; -1 = skip), accumulated
+// from +0 in slot order with __fmaf_rn and rounded once with
+// __floats2bfloat162_rn.  The same kernel serves the contiguous layout
+// (rows of [R, cap_rows]) and the packed layout (rows of [E, R*max]).
+//
+// One warp handles one (token, 512-channel segment) item: every lane issues
+// all k row loads of its 2 x 16 bytes before the first fma (k*2 independent
+// 16-byte streaming loads in flight per lane), then reduces in registers and
+// stores 2 x 16 bytes of bf16.  Rows are read whole and in order, so every
+// warp load instruction moves 512 contiguous bytes.
+
+#include "ep_common.cuh"
+
+namespace ep {
+
+constexpr int kCombineThreads = 256;
+
+struct CombineParams {
+  const uint8_t* y;
+  const float* w;
+  const int32_t* cidx;
+  int64_t n_rows;
+  int64_t T;
+  int H, k, nseg;
+  uint8_t* out;
+  int32_t* status;
+};
+
+template <int kU, int kK>
+__global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineParams p) {
+  constexpr int kSegC = kU * kWarp * 8;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kCombineThreads) >> 5;
+  const int64_t row_bytes = (int64_t)p.H * 2;
+
+  for (int64_t it = warp0; it < (int64_t)p.T * p.nseg; it += nwarps) {
+    const int64_t g = it / p.nseg;
+    const int s = (int)(it - g * p.nseg);
+    const int ch0 = s * kSegC;
+
+    int32_t my_f = -1;
+    float my_w = 0.0f;
+    if (lane < p.k) {
+      my_f = p.cidx[g * p.k + lane];
+      my_w = p.w[g * p.k + lane];
+      if (my_f < -1 || (int64_t)my_f >= p.n_rows) {
+        if (s == 0) set_status(p.status, EP_ERR_INVALID_ARG);
+        my_f = -1;
+      }
+    }
+    int32_t f[kK];
+    float wt[kK];
+#pragma unroll
+    for (int j = 0; j < kK; ++j) {
+      f[j] = __shfl_sync(0xffffffffu, my_f, j);
+      wt[j] = __shfl_sync(0xffffffffu, my_w, j);
+    }
+
+    uint4 v[kU][kK];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int ch = ch0 + u * 256 + lane * 8;
+#pragma unroll
+      for (int j = 0; j < kK; ++j) {
+        if (j < p.k && f[j] >= 0 && ch < p.H)
+          v[u][j] = ld_stream_v4(p.y + (int64_t)f[j] * row_bytes + (int64_t)ch * 2);
+        else
+          v[u][j] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int ch = ch0 + u * 256 + lane * 8;
+      float acc[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kK; ++j) {
+        if (j < p.k && f[j] >= 0) {
+          const uint4 a = v[u][j];
+          acc[0] = __fmaf_rn(wt[j], bf16_lo(a.x), acc[0]);
+          acc[1] = __fmaf_rn(wt[j], bf16_hi(a.x), acc[1]);
+          acc[2] = __fmaf_rn(wt[j], bf16_lo(a.y), acc[2]);
+          acc[3] = __fmaf_rn(wt[j], bf16_hi(a.y), acc[3]);
+          acc[4] = __fmaf_rn(wt[j], bf16_lo(a.z), acc[4]);
+          acc[5] = __fmaf_rn(wt[j], bf16_hi(a.z), acc[5]);
+          acc[6] = __fmaf_rn(wt[j], bf16_lo(a.w), acc[6]);
+          acc[7] = __fmaf_rn(wt[j], bf16_hi(a.w), acc[7]);
+        }
+      }
+      if (ch < p.H) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        st_v4(p.out + g * row_bytes + (int64_t)ch * 2, o);
+      }
+    }
+  }
+}
+
+template <int kU, int kK>
+static int launch_combine_t(const CombineParams& p, cudaStream_t stream) {
+  constexpr int kSegC = kU * kWarp * 8;
+  CombineParams q = p;
+  q.nseg = (p.H + kSegC - 1) / kSegC;
+  const int64_t items = q.T * q.nseg;
+  if (items == 0) return EP_OK;
+  const int64_t want = (items + (kCombineThreads / kWarp) - 1) / (kCombineThreads / kWarp);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::num_sms() * 2));
+  k_combine<kU, kK><<<grid, kCombineThreads, 0, stream>>>(q);
+  ep_host::count_launch();
+  return ep_host::check_launch();
+}
+
+static int launch_combine(const CombineParams& p, cudaStream_t stream) {
+  if (p.k <= 8) return launch_combine_t<2, 8>(p, stream);
+  return launch_combine_t<1, 16>(p, stream);
+}
+
+static int check_combine(const void* y, const float* w, const int32_t* cidx, int R, int T_r, int H,
+                         int k, const void* out) {
+  if (R <= 0 || R > kMaxR || T_r < 0 || H <= 0 || H % 8 != 0 || k <= 0 || k > kMaxK)
+    return EP_ERR_INVALID_ARG;
+  if (T_r > 0 && (!y || !w || !cidx || !out)) return EP_ERR_INVALID_ARG;
+  if (!ep_host::aligned16(y) || !ep_host::aligned16(out)) return EP_ERR_INVALID_ARG;
+  return EP_OK;
+}
+
+}  // namespace ep
+
+extern "C" int ep_combine(const void* y, const float* topk_weights, const int32_t* combine_idx,
+                          int R, int T_r, int H, int k, int64_t cap_rows, void* out,
+                          int32_t* status, void* stream) {
+  int rc = ep::check_combine(y, topk_weights, combine_idx, R, T_r, H, k, out);
+  if (rc != EP_OK) return rc;
+  if (cap_rows < 0) return EP_ERR_INVALID_ARG;
+  ep::CombineParams p{};
+  p.y = static_cast<const uint8_t*>(y);
+  p.w = topk_weights;
+  p.cidx = combine_idx;
+  p.n_rows = (int64_t)R * cap_rows;
+  p.T = (int64_t)R * T_r;
+  p.H = H;
+  p.k = k;
+  p.out = static_cast<uint8_t*>(out);
+  p.status = status;
+  return ep::launch_combine(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ep_ll_combine(const void* y, const float* topk_weights, const int32_t* combine_idx,
+                             int R, int T_r, int H, int E, int k, int max_tokens_per_rank,
+                             void* out, int32_t* status, void* stream) {
+  int rc = ep::check_combine(y, topk_weights, combine_idx, R, T_r, H, k, out);
+  if (rc != EP_OK) return rc;
+  if (E <= 0 || E % R != 0 || max_tokens_per_rank <= 0) return EP_ERR_INVALID_ARG;
+  ep::CombineParams p{};
+  p.y = static_cast<const uint8_t*>(y);
+  p.w = topk_weights;
+  p.cidx = combine_idx;
+  p.n_rows = (int64_t)E * R * max_tokens_per_rank;
+  p.T = (int64_t)R * T_r;
+  p.H = H;
+  p.k = k;
+  p.out = static_cast<uint8_t*>(out);
+  p.status = status;
+  return ep::launch_combine(p, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,364 @@
+// layout.cu -- routing layout: per-rank / per-expert counts, is_token_in_rank
+// and the deterministic slot ranks, in ONE pass over topk_idx.
+//
+// get_dispatch_layout (llm-infra-atlas DeepEP article, §2.1) counts, per
+// source rank, the tokens for every rank and the slots for every expert.
+// The contiguous and packed layouts (§1.1, §1.2, §2.3) additionally need, for
+// each slot, its position among the slots routed to the same expert -- the
+// row offset the receiver uses.  That is a segmented exclusive scan over
+// T*k ids with E buckets, done here as one kernel:
+//   1. a CTA takes a chunk of tokens (claimed through an atomic ticket, so
+//      chunks start in order and every wait below is on an earlier,
+//      already-running CTA), ranks its ids per warp with __match_any_sync
+//      and reduces the per-warp counts in shared memory;
+//   2. it publishes the chunk aggregate and looks back over the previous
+//      chunks' published (aggregate | inclusive) words, 8 at a time, to get
+//      its exclusive prefix per expert (decoupled look-back);
+//   3. it writes the per-slot results.
+// Normal mode scans within each source rank (get_dispatch_layout is a
+// per-rank operation).  Low-latency mode scans across all ranks in
+// (rank, token, slot) order, which directly yields the packed row
+// expert_prefix[i][e] + slot_rank (§1.2, §3.2), so ep_ll_dispatch needs no
+// separate notify step -- the V2 design of §4.6 (counting fused into the
+// dispatch launch, no CPU round trip).
+//
+// Every wait is bounded by kWaitNs of %globaltimer; on expiry the CTA
+// records EP_ERR_TIMEOUT, treats the missing value as 0 and carries on, so
+// no CTA can hang.  Look-back words carry a launch epoch, so the workspace
+// needs no clearing between launches.
+
+#include "ep_common.cuh"
+#include "layout.cuh"
+
+namespace ep {
+
+constexpr int kLayoutThreads = 256;
+constexpr int kLayoutWarps = kLayoutThreads / kWarp;
+constexpr int kMaxChunkIds = 2048;
+constexpr int kIdsPerLane = kMaxChunkIds / kLayoutThreads;   // 8
+constexpr int kLookbackWindow = 8;
+
+enum : uint32_t { kFlagAggregate = 1, kFlagInclusive = 2 };
+
+__device__ __forceinline__ uint64_t pack_flag(uint32_t epoch, uint32_t kind, uint32_t value) {
+  return ((uint64_t)((epoch << 2) | kind) << 32) | value;
+}
+
+// Wait (bounded) until a look-back word of this launch is published.  A wait
+// gives up after kWaitNs, or at once when another CTA already gave up (the
+// workspace's abort word), so a broken launch ends after one bound rather
+// than one bound per predecessor.  Giving up records EP_ERR_TIMEOUT and
+// counts the missing value as 0.
+__device__ __forceinline__ uint64_t wait_flag(const uint64_t* addr, uint64_t f, uint32_t epoch,
+                                              uint32_t* abort_word, int32_t* status) {
+  const uint32_t tag_a = (epoch << 2) | kFlagAggregate;
+  const uint32_t tag_i = (epoch << 2) | kFlagInclusive;
+  uint32_t tag = (uint32_t)(f >> 32);
+  if (tag == tag_a || tag == tag_i) return f;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (ld_relaxed_u32(abort_word) != 0u) break;
+    __nanosleep(40);
+    f = ld_relaxed_u64(addr);
+    tag = (uint32_t)(f >> 32);
+    if (tag == tag_a || tag == tag_i) return f;
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      atomicExch(abort_word, 1u);
+      break;
+    }
+  }
+  set_status(status, EP_ERR_TIMEOUT);
+  return pack_flag(epoch, kFlagAggregate, 0);
+}
+
+template <bool kLL>
+__global__ void __launch_bounds__(kLayoutThreads) k_layout(LayoutParams p) {
+  extern __shared__ int32_t smem[];
+  int32_t* s_ids = smem;                                  // [kMaxChunkIds]
+  int32_t* s_cnt = s_ids + kMaxChunkIds;                  // [warps][E]
+  int32_t* s_agg = s_cnt + kLayoutWarps * p.E;            // [V]
+  int32_t* s_excl = s_agg + p.V;                          // [V]
+  __shared__ uint32_t s_ticket, s_epoch;
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+
+  if (kLL) pdl_launch_dependents();   // the scatter kernel may start loading x
+  if (tid == 0) {
+    s_ticket = atomicAdd(&p.ctl[0], 1u);
+    s_epoch = ld_relaxed_u32(&p.ctl[2]);
+  }
+  for (int v = tid; v < kLayoutWarps * p.E; v += kLayoutThreads) s_cnt[v] = 0;
+  for (int v = p.E + tid; v < p.V; v += kLayoutThreads) s_agg[v] = 0;
+  __syncthreads();
+
+  const uint32_t b = s_ticket;
+  const uint32_t epoch = s_epoch & 0x3fffffffu;
+  if (b >= (uint32_t)p.num_chunks) {   // workspace not cleaned: give up loudly
+    if (tid == 0) {
+      atomicExch(&p.ctl[3], 1u);
+      set_status(p.status, EP_ERR_STATE);
+    }
+    return;
+  }
+  const int i = (int)b / p.chunks_per_rank;
+  const int c = (int)b % p.chunks_per_rank;
+  const int t0 = c * p.chunk_tokens;
+  const int nt = max(0, min(p.chunk_tokens, p.T_r - t0));
+  const int n = nt * p.k;
+  const int64_t id_base = ((int64_t)i * p.T_r + t0) * p.k;
+
+  // ---- 1. load the chunk's ids (validated) into shared memory
+  for (int q = tid; q < n; q += kLayoutThreads) {
+    int64_t e = p.topk_idx[id_base + q];
+    int v = -1;
+    if (e >= 0 && e < p.E) v = (int)e;
+    else if (e != -1) set_status(p.status, EP_ERR_INVALID_ARG);
+    s_ids[q] = v;
+  }
+  __syncthreads();
+
+  // ---- per-warp ranks: warp w owns a contiguous run of the chunk's ids
+  const int per_warp = ((n + kLayoutThreads - 1) / kLayoutThreads) * kWarp;
+  const int wbase = warp * per_warp;
+  int my_rank[kIdsPerLane];
+#pragma unroll
+  for (int u = 0; u < kIdsPerLane; ++u) {
+    my_rank[u] = 0;
+    if (u * kWarp < per_warp) {
+      const int q = wbase + u * kWarp + lane;
+      const int e = (q < n) ? s_ids[q] : -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      int r = 0;
+      if (e >= 0) r = s_cnt[warp * p.E + e] + __popc(peers & lanemask_lt());
+      __syncwarp();
+      if (e >= 0 && (__ffs(peers) - 1) == lane) s_cnt[warp * p.E + e] += __popc(peers);
+      __syncwarp();
+      my_rank[u] = r;
+    }
+  }
+  __syncthreads();
+
+  // ---- chunk aggregate per expert; per-warp counts become warp offsets
+  for (int e = tid; e < p.E; e += kLayoutThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kLayoutWarps; ++w) {
+      const int tmp = s_cnt[w * p.E + e];
+      s_cnt[w * p.E + e] = run;
+      run += tmp;
+    }
+    s_agg[e] = run;
+  }
+  // ---- normal mode: is_token_in_rank and tokens per destination rank
+  if (!kLL) {
+    for (int tt = tid; tt < nt; tt += kLayoutThreads) {
+      const int32_t* te = s_ids + tt * p.k;
+      uint8_t* row = p.is_token_in_rank + ((int64_t)i * p.T_r + t0 + tt) * p.R;
+      int dst[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) dst[j] = (j < p.k && te[j] >= 0) ? te[j] / p.E_l : -1;
+      for (int r = 0; r < p.R; ++r) {
+        bool hit = false;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) hit |= (dst[j] == r);
+        row[r] = hit ? 1 : 0;
+        if (hit) atomicAdd(&s_agg[p.E + r], 1);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- 2. publish the aggregate, look back for the exclusive prefix
+  const int seq_first = kLL ? 0 : i * p.chunks_per_rank;
+  uint64_t* F = p.flags;
+  if ((int)b == seq_first) {
+    for (int v = tid; v < p.V; v += kLayoutThreads) {
+      s_excl[v] = 0;
+      st_relaxed_u64(&F[(size_t)b * p.V + v], pack_flag(epoch, kFlagInclusive, (uint32_t)s_agg[v]));
+    }
+  } else {
+    for (int v = tid; v < p.V; v += kLayoutThreads)
+      st_relaxed_u64(&F[(size_t)b * p.V + v], pack_flag(epoch, kFlagAggregate, (uint32_t)s_agg[v]));
+    for (int v = tid; v < p.V; v += kLayoutThreads) {
+      uint32_t excl = 0;
+      int pp = (int)b - 1;
+      bool done = false;
+      while (!done && pp >= seq_first) {
+        const int nw = min(kLookbackWindow, pp - seq_first + 1);
+        uint64_t wv[kLookbackWindow];
+#pragma unroll
+        for (int q = 0; q < kLookbackWindow; ++q)
+          if (q < nw) wv[q] = ld_relaxed_u64(&F[(size_t)(pp - q) * p.V + v]);
+#pragma unroll
+        for (int q = 0; q < kLookbackWindow; ++q) {
+          if (q < nw && !done) {
+            const uint64_t f =
+                wait_flag(&F[(size_t)(pp - q) * p.V + v], wv[q], epoch, &p.ctl[3], p.status);
+            excl += (uint32_t)f;
+            if ((uint32_t)(f >> 32) == ((epoch << 2) | kFlagInclusive)) done = true;
+          }
+        }
+        pp -= nw;
+      }
+      s_excl[v] = (int32_t)excl;
+      st_relaxed_u64(&F[(size_t)b * p.V + v],
+                     pack_flag(epoch, kFlagInclusive, excl + (uint32_t)s_agg[v]));
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. per-slot outputs
+#pragma unroll
+  for (int u = 0; u < kIdsPerLane; ++u) {
+    if (u * kWarp < per_warp) {
+      const int q = wbase + u * kWarp + lane;
+      if (q < n) {
+        const int e = s_ids[q];
+        const int64_t pos = id_base + q;
+        if (kLL) {
+          int32_t out = -1;
+          if (e >= 0) {
+            const int64_t row = (int64_t)s_excl[e] + s_cnt[warp * p.E + e] + my_rank[u];
+            if (row >= 0 && row < p.seg_rows) {
+              const int64_t f = (int64_t)e * p.seg_rows + row;
+              out = (int32_t)f;
+              p.src_info[f] = i * p.T_r + t0 + q / p.k;
+            } else {
+              set_status(p.status, EP_ERR_CAPACITY);
+            }
+          }
+          p.combine_idx[pos] = out;
+        } else {
+          p.slot_rank[pos] = (e >= 0) ? s_excl[e] + s_cnt[warp * p.E + e] + my_rank[u] : -1;
+        }
+      }
+    }
+  }
+  if (c == p.chunks_per_rank - 1) {     // last chunk of rank i: rank totals
+    if (kLL) {
+      for (int e = tid; e < p.E; e += kLayoutThreads)
+        p.rank_end[(size_t)i * p.E + e] = s_excl[e] + s_agg[e];
+    } else {
+      for (int e = tid; e < p.E; e += kLayoutThreads)
+        p.num_tokens_per_expert[(size_t)i * p.E + e] = s_excl[e] + s_agg[e];
+      for (int r = tid; r < p.R; r += kLayoutThreads)
+        p.num_tokens_per_rank[(size_t)i * p.R + r] = s_excl[p.E + r] + s_agg[p.E + r];
+    }
+  }
+  if (kLL && c == 0) {
+    for (int e = tid; e < p.E; e += kLayoutThreads) p.rank_start[(size_t)i * p.E + e] = s_excl[e];
+  }
+
+  // ---- the last CTA to finish resets the ticket state (and, in low-latency
+  //      mode, writes recv_count and layout_range from the rank boundaries)
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t d = atomicAdd(&p.ctl[1], 1u);
+    s_last = (d == (uint32_t)p.num_chunks - 1);
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    if (kLL) {
+      for (int e = tid; e < p.E; e += kLayoutThreads) {
+        for (int r = 0; r < p.R; ++r) {
+          const int32_t lo = ld_cg_i32(&p.rank_start[(size_t)r * p.E + e]);
+          const int32_t hi = ld_cg_i32(&p.rank_end[(size_t)r * p.E + e]);
+          p.layout_range[(size_t)e * p.R + r] = ((int64_t)lo << 32) | (int64_t)(uint32_t)(hi - lo);
+        }
+        p.recv_count[e] = ld_cg_i32(&p.rank_end[(size_t)(p.R - 1) * p.E + e]);
+      }
+    }
+    if (tid == 0) {
+      p.ctl[0] = 0;
+      p.ctl[1] = 0;
+      p.ctl[2] = s_epoch + 1;
+      p.ctl[3] = 0;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+LayoutGeometry layout_geometry(int R, int T_r, int k, int E) {
+  LayoutGeometry g;
+  g.chunk_tokens = kMaxChunkIds / k;
+  g.chunks_per_rank = T_r > 0 ? (T_r + g.chunk_tokens - 1) / g.chunk_tokens : 1;
+  g.num_chunks = (int64_t)R * g.chunks_per_rank;
+  g.V = E + R;
+  g.flags_offset = 256;
+  g.rank_start_offset = g.flags_offset + (size_t)g.num_chunks * g.V * sizeof(uint64_t);
+  g.rank_end_offset = g.rank_start_offset + (size_t)R * E * sizeof(int32_t);
+  g.bytes = (g.rank_end_offset + (size_t)R * E * sizeof(int32_t) + 255) / 256 * 256;
+  return g;
+}
+
+static size_t layout_smem_bytes(int E, int V) {
+  return sizeof(int32_t) * ((size_t)kMaxChunkIds + (size_t)kLayoutWarps * E + 2 * (size_t)V);
+}
+
+int launch_layout(const LayoutParams& p_in, bool ll, void* ws, cudaStream_t stream) {
+  LayoutParams p = p_in;
+  char* base = static_cast<char*>(ws);
+  const LayoutGeometry g = layout_geometry(p.R, p.T_r, p.k, p.E);
+  p.ctl = reinterpret_cast<uint32_t*>(base);
+  p.flags = reinterpret_cast<uint64_t*>(base + g.flags_offset);
+  p.rank_start = reinterpret_cast<int32_t*>(base + g.rank_start_offset);
+  p.rank_end = reinterpret_cast<int32_t*>(base + g.rank_end_offset);
+  p.chunk_tokens = g.chunk_tokens;
+  p.chunks_per_rank = g.chunks_per_rank;
+  p.num_chunks = (int)g.num_chunks;
+  p.V = ll ? p.E : p.E + p.R;
+  const size_t smem = layout_smem_bytes(p.E, p.V);
+  auto kern = ll ? k_layout<true> : k_layout<false>;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[ll]) {
+    const int max_smem = (int)layout_smem_bytes(kMaxE, kMaxE + kMaxR);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+        cudaSuccess)
+      return EP_ERR_CUDA;
+    attr_set[ll] = true;
+  }
+  kern<<<p.num_chunks, kLayoutThreads, smem, stream>>>(p);
+  ep_host::count_launch();
+  return ep_host::check_launch();
+}
+
+}  // namespace ep
+
+extern "C" size_t ep_workspace_size(int R, int T_r, int k, int E) {
+  if (R <= 0 || k <= 0 || k > ep::kMaxK || E <= 0 || T_r < 0) return 0;
+  return ep::layout_geometry(R, T_r, k, E).bytes;
+}
+
+extern "C" int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E,
+                                      int32_t* num_tokens_per_rank,
+                                      int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                                      int32_t* slot_rank, void* workspace, size_t workspace_bytes,
+                                      int32_t* status, void* stream) {
+  if (R <= 0 || R > ep::kMaxR || E <= 0 || E > ep::kMaxE || E % R != 0 || k <= 0 ||
+      k > ep::kMaxK || T_r < 0)
+    return EP_ERR_INVALID_ARG;
+  if (!num_tokens_per_rank || !num_tokens_per_expert || !workspace ||
+      (T_r > 0 && (!topk_idx || !is_token_in_rank || !slot_rank)))
+    return EP_ERR_INVALID_ARG;
+  if (workspace_bytes < ep_workspace_size(R, T_r, k, E)) return EP_ERR_INVALID_ARG;
+  ep::LayoutParams p{};
+  p.topk_idx = topk_idx;
+  p.R = R;
+  p.T_r = T_r;
+  p.k = k;
+  p.E = E;
+  p.E_l = E / R;
+  p.num_tokens_per_rank = num_tokens_per_rank;
+  p.num_tokens_per_expert = num_tokens_per_expert;
+  p.is_token_in_rank = is_token_in_rank;
+  p.slot_rank = slot_rank;
+  p.status = status;
+  return ep::launch_layout(p, false, workspace, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,47 @@
+// layout.cuh -- parameters of the layout kernel (see layout.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ep {
+
+struct LayoutParams {
+  const int64_t* topk_idx;
+  int R, T_r, k, E, E_l;
+  int chunk_tokens, chunks_per_rank, num_chunks, V;
+  // normal-mode outputs (get_dispatch_layout)
+  int32_t* num_tokens_per_rank;
+  int32_t* num_tokens_per_expert;
+  uint8_t* is_token_in_rank;
+  int32_t* slot_rank;
+  // low-latency outputs (packed rows)
+  int32_t* combine_idx;
+  int32_t* src_info;
+  int32_t* recv_count;
+  int64_t* layout_range;
+  int64_t seg_rows;
+  // workspace views
+  uint32_t* ctl;        // [0] ticket, [1] finished CTAs, [2] launch epoch, [3] abort
+  uint64_t* flags;      // [num_chunks][V] look-back words
+  int32_t* rank_start;  // [R][E] low-latency: prefix at the start of each rank
+  int32_t* rank_end;    // [R][E] low-latency: prefix at the end of each rank
+  int32_t* status;
+};
+
+struct LayoutGeometry {
+  int chunk_tokens;
+  int chunks_per_rank;
+  int64_t num_chunks;
+  int V;
+  size_t flags_offset, rank_start_offset, rank_end_offset, bytes;
+};
+
+LayoutGeometry layout_geometry(int R, int T_r, int k, int E);
+
+// Launch the layout kernel on workspace `ws` (normal: per-rank scan into
+// p's normal outputs; ll: global scan into p's low-latency outputs).
+int launch_layout(const LayoutParams& p, bool ll, void* ws, cudaStream_t stream);
+
+}  // namespace ep

@@ -145,8 +145,7 @@ def expert_outputs_torch(n_rows: int, H: int, device, seed: int = 0) -> torch.Te
     """Stand-in expert outputs y [n_rows, H] bf16 ~ N(0,1) on `device`."""
     g = torch.Generator(device=device)
     g.manual_seed(seed * 1000003 + 29)
-    return torch.randn((n_rows, H), generator=g, device=device,
-                       dtype=torch.float32).to(torch.bfloat16)
+    return torch.randn((n_rows, H), generator=g, device=device, dtype=torch.bfloat16)
 
 
 def expert_outputs(n_rows: int, H: int, seed: int = 0) -> np.ndarray:

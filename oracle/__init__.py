@@ -180,7 +180,12 @@ def notify(num_tokens_per_rank: np.ndarray, num_tokens_per_expert: np.ndarray, R
     return out
 
 
-def _recv_buffers(n_seg: int, seg_rows: int, H: int, fp8_mode: int, fill: int):
+def _recv_buffers(n_seg: int, seg_rows: int, H: int, fp8_mode: int, fill):
+    if fill is None:        # lazily mapped: only rows the oracle writes are touched
+        recv = np.empty((n_seg, seg_rows, H), np.uint16 if fp8_mode == FP8_NONE else np.uint8)
+        sdt = np.float32 if fp8_mode == FP8_E4M3_F32_SCALE else np.uint8
+        scales = None if fp8_mode == FP8_NONE else np.empty((n_seg, H // 128, seg_rows), sdt)
+        return recv, scales
     if fp8_mode == FP8_NONE:
         recv = np.full((n_seg, seg_rows, H), fill & 0xFFFF, np.uint16)
         scales = None

@@ -1,0 +1,153 @@
+"""GPU parity: normal-mode dispatch (contiguous per-expert layout, bf16 or
+fused FP8) vs the oracle -- bit-exact rows, scales and indices."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_get_dispatch_gb300 import ep, synth
+from ep_harness import (POISON, gpu_dispatch, gpu_layout, gpu_notify, inputs, np_, oracle_normal,
+                        status_word, to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_both(w, A=1, cap_rows=None, x_on_device=False):
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w, x_on_device=x_on_device)
+    lay = gpu_layout(idx_dev, w.E)
+    nt = gpu_notify(lay, w.E, A, w.num_worst_tokens)
+    ref_lay = oracle.layout(idx, w.R, w.E)
+    ref_nt = oracle.notify(ref_lay["num_tokens_per_rank"], ref_lay["num_tokens_per_expert"], w.R,
+                           w.E, A, w.num_worst_tokens)
+    if cap_rows is None:
+        cap_rows = (w.cap_rows() if w.num_worst_tokens >= 0
+                    else max(1, int(ref_nt["psum"][:, -1].max())))
+    d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, w.fp8_mode, cap_rows)
+    return x_dev, x_host, idx, lay, nt, d, cap_rows
+
+
+def _compare_full(w, x_host, idx, d, cap_rows, A):
+    _, _, ref, _ = oracle_normal(x_host, idx, w.E, A, w.fp8_mode, cap_rows=cap_rows,
+                                 num_worst_tokens=w.num_worst_tokens)
+    assert ref["rc"] == oracle.OK
+    assert np.array_equal(np_(d["combine_idx"]), ref["combine_idx"])
+    src = np_(d["recv_src_idx"])
+    assert np.array_equal(src, ref["recv_src_idx"])
+    rows = np.nonzero(src.reshape(-1) >= 0)[0]
+    got = np_(d["recv_x"]).reshape(w.R * cap_rows, -1)
+    assert np.array_equal(got[rows], ref["recv_x"].reshape(w.R * cap_rows, -1)[rows])
+    # rows nobody fills stay untouched (poison)
+    unused = np.nonzero(src.reshape(-1) < 0)[0]
+    if unused.size:
+        assert np.all(got[unused[:4096]].view(np.uint8) == POISON)
+    if w.fp8_mode:
+        gs = np_(d["recv_scales"])                         # [R, H/128, cap]
+        rs = ref["recv_scales"]
+        r_idx, row_idx = np.divmod(rows, cap_rows)
+        assert np.array_equal(gs[r_idx, :, row_idx], rs[r_idx, :, row_idx])
+
+
+@pytest.mark.parametrize("fp8_mode", [0, 1, 2])
+@pytest.mark.parametrize("A", [1, 128])
+def test_dispatch_tiny(fp8_mode, A):
+    w = synth.scaled(synth.WORKLOADS["tiny"], fp8_mode=fp8_mode)
+    x_dev, x_host, idx, lay, nt, d, cap = _run_both(w, A)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_full(w, x_host, idx, d, cap, A)
+
+
+@pytest.mark.parametrize("name,T_r,fp8_mode", [
+    ("prefill", 96, 0), ("prefill", 96, 2), ("skewed", 40, 1), ("large", 80, 2), ("decode", 16, 1),
+])
+def test_dispatch_scaled_full_compare(name, T_r, fp8_mode):
+    base = synth.WORKLOADS[name]
+    nwt = base.R * T_r if base.num_worst_tokens >= 0 else -1
+    w = synth.scaled(base, T_r=T_r, fp8_mode=fp8_mode, num_worst_tokens=nwt)
+    x_dev, x_host, idx, lay, nt, d, cap = _run_both(w, 1)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_full(w, x_host, idx, d, cap, 1)
+
+
+@pytest.mark.parametrize("H", [8, 136, 1032, 1024 + 512 + 8])
+def test_dispatch_bf16_ragged_hidden(H):
+    w = synth.scaled(synth.WORKLOADS["tiny"], H=H, T_r=33)
+    x_dev, x_host, idx, lay, nt, d, cap = _run_both(w, 4)
+    _compare_full(w, x_host, idx, d, cap, 4)
+
+
+@pytest.mark.parametrize("H", [128, 384, 1152])
+@pytest.mark.parametrize("fp8_mode", [1, 2])
+def test_dispatch_fp8_small_hidden_and_zero_rows(H, fp8_mode):
+    w = synth.scaled(synth.WORKLOADS["tiny"], H=H, T_r=20, fp8_mode=fp8_mode)
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
+    x_host = x_host.copy()
+    x_host[0, 3] = 0                                     # all-zero row: amax floor
+    x_host[1, 5, :128] = 0x8000                          # -0.0 block
+    x_host[2, 7, ::2] = synth.to_bf16_bits(np.float32([3e38]))[0]   # near bf16 max
+    x_host[3, 9] = synth.to_bf16_bits(np.float32([1e-30]))[0]       # tiny values
+    x_dev = to_dev_bf16(x_host)
+    lay = gpu_layout(idx_dev, w.E)
+    nt = gpu_notify(lay, w.E, 1)
+    cap = int(np_(nt["psum"])[:, -1].max())
+    d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, fp8_mode, cap)
+    _compare_full(w, x_host, idx, d, cap, 1)
+
+
+def test_dispatch_masked_slots_and_capacity_overflow():
+    w = synth.WORKLOADS["tiny"]
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
+    idx = idx.copy()
+    idx[0, :4, 1] = -1
+    idx[2, 5, :] = -1
+    idx_dev = torch.from_numpy(idx).cuda()
+    lay = gpu_layout(idx_dev, w.E)
+    nt = gpu_notify(lay, w.E, 1)
+    full = int(np_(nt["psum"])[:, -1].max())
+    d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, 0, full)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_full(w, x_host, idx, d, full, 1)
+    small = full - 3
+    d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, 0, small)
+    assert ep.ep_read_status(d["status"]) == ep.EP_ERR_CAPACITY
+    _, _, ref, _ = oracle_normal(x_host, idx, w.E, 1, 0, cap_rows=small)
+    assert ref["rc"] == oracle.ERR_CAPACITY
+    assert np.array_equal(np_(d["combine_idx"]), ref["combine_idx"])
+    assert np.array_equal(np_(d["recv_src_idx"]), ref["recv_src_idx"])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["prefill", "skewed", "large"])
+def test_dispatch_full_size_sampled(name):
+    """Full-size workloads in the bench's launch configuration: all index
+    outputs compared whole, data rows of a random sample of tokens compared
+    against the oracle's per-row definition."""
+    w = synth.WORKLOADS[name]
+    x_dev, x_host, idx, lay, nt, d, cap = _run_both(w, 1, x_on_device=True)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    ref_lay = oracle.layout(idx, w.R, w.E)
+    ref_nt = oracle.notify(ref_lay["num_tokens_per_rank"], ref_lay["num_tokens_per_expert"], w.R,
+                           w.E, 1, w.num_worst_tokens)
+    # indices: the oracle's dispatch with zero-width rows (no row data to move)
+    x0 = np.zeros((w.R, w.T_r, 0), np.uint16)
+    ref = oracle.dispatch(x0, idx, ref_lay["slot_rank"], ref_nt["expert_prefix"], ref_nt["psum"],
+                          w.E, 0, cap)
+    assert ref["rc"] == oracle.OK
+    ref_cidx = ref["combine_idx"]
+    assert np.array_equal(np_(d["combine_idx"]), ref_cidx)
+    assert np.array_equal(np_(d["recv_src_idx"]), ref["recv_src_idx"])
+    # sampled rows
+    rng = np.random.default_rng(11)
+    toks = rng.choice(w.T, size=min(192, w.T), replace=False)
+    recv = d["recv_x"].view(w.R * cap, -1)
+    for g in toks:
+        i, t = divmod(int(g), w.T_r)
+        for j in range(w.k):
+            f = int(ref_cidx[i, t, j])
+            got = np_(recv[f])
+            if w.fp8_mode == 0:
+                assert np.array_equal(got, x_host[i, t])
+            else:
+                q, s = oracle.quantize_row(x_host[i, t], w.fp8_mode)
+                assert np.array_equal(got, q)
+                rr, rw = divmod(f, cap)
+                assert np.array_equal(np_(d["recv_scales"][rr, :, rw]), s)

@@ -1,0 +1,130 @@
+"""GPU parity: low-latency dispatch into the packed masked layout vs the
+oracle (bit-exact rows, scales, counts, ranges, indices), the bounded
+device waits of its layout pass, and ep_clean_ll_buffer."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_get_dispatch_gb300 import ep, synth
+from ep_harness import POISON, gpu_ll_dispatch, inputs, np_, status_word
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare_ll(w, x_host, idx, d, max_tokens, fp8_mode):
+    ref = oracle.ll_dispatch(x_host, idx, w.E, max_tokens, fp8_mode)
+    assert ref["rc"] == oracle.OK
+    S = w.R * max_tokens
+    assert np.array_equal(np_(d["recv_count"]), ref["recv_count"])
+    assert np.array_equal(np_(d["layout_range"]), ref["layout_range"])
+    assert np.array_equal(np_(d["combine_idx"]), ref["combine_idx"])
+    cnt = ref["recv_count"].reshape(-1)
+    src = np_(d["packed_recv_src_info"]).reshape(w.E, S)
+    px = np_(d["packed_recv_x"]).reshape(w.E, S, -1)
+    rsrc = ref["packed_recv_src_info"].reshape(w.E, S)
+    rpx = ref["packed_recv_x"].reshape(w.E, S, -1)
+    for e in range(w.E):
+        c = cnt[e]
+        assert np.array_equal(src[e, :c], rsrc[e, :c]), e
+        assert np.array_equal(px[e, :c], rpx[e, :c]), e
+        if c < S:   # rows past recv_count are untouched
+            assert np.all(px[e, c:c + 2].view(np.uint8) == POISON)
+            assert np.all(src[e, c:c + 2].view(np.uint8) == POISON)
+    if fp8_mode:
+        ps = np_(d["packed_recv_scales"]).reshape(w.E, w.H // 128, S)
+        rps = ref["packed_recv_scales"].reshape(w.E, w.H // 128, S)
+        for e in range(w.E):
+            assert np.array_equal(ps[e, :, :cnt[e]], rps[e, :, :cnt[e]]), e
+
+
+@pytest.mark.parametrize("fp8_mode", [0, 1, 2])
+def test_ll_tiny(fp8_mode):
+    w = synth.scaled(synth.WORKLOADS["tiny"], fp8_mode=fp8_mode)
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, fp8_mode)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_ll(w, x_host, idx, d, w.max_tokens_per_rank, fp8_mode)
+
+
+@pytest.mark.slow
+def test_ll_decode_full_size():
+    """The decode workload exactly as the benchmark runs it."""
+    w = synth.WORKLOADS["decode"]
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, w.fp8_mode)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_ll(w, x_host, idx, d, w.max_tokens_per_rank, w.fp8_mode)
+    # a second call on the same workspace gives identical results
+    d2 = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, w.fp8_mode, ws=d["ws"])
+    for key in ("recv_count", "layout_range", "combine_idx"):
+        assert torch.equal(d2[key], d[key]), key
+
+
+@pytest.mark.parametrize("R,T_r,max_tokens,k,E,H,fp8_mode", [
+    (16, 100, 128, 8, 256, 1024, 2),   # T_r below the per-rank capacity
+    (4, 700, 700, 4, 32, 256, 1),      # several chunks per rank (ragged)
+    (8, 1, 1, 1, 8, 128, 0),           # one token per rank, one expert per rank
+    (2, 0, 4, 2, 4, 128, 2),           # no tokens at all
+    (32, 256, 256, 6, 128, 4096, 1),   # the skewed workload's shape, low-latency
+])
+def test_ll_shapes(R, T_r, max_tokens, k, E, H, fp8_mode):
+    w = synth.Workload("t", R=R, T_r=T_r, H=H, E=E, k=k, routing="uniform", mode="ll",
+                       fp8_mode=fp8_mode, max_tokens_per_rank=max_tokens)
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
+    d = gpu_ll_dispatch(x_dev, idx_dev, E, max_tokens, fp8_mode)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_ll(w, x_host, idx, d, max_tokens, fp8_mode)
+
+
+def test_ll_masked_and_repeated_experts_capacity():
+    R, T_r, k, E, H = 2, 2, 2, 4, 128
+    w = synth.Workload("t", R=R, T_r=T_r, H=H, E=E, k=k, routing="uniform", mode="ll",
+                       fp8_mode=0, max_tokens_per_rank=2)
+    x_dev, x_host, _, _, _, _ = inputs(w)
+    idx = np.zeros((R, T_r, k), np.int64)      # 8 slots to expert 0, room for 4
+    idx[1, 1, 1] = -1
+    d = gpu_ll_dispatch(x_dev, torch.from_numpy(idx).cuda(), E, 2, 0)
+    assert ep.ep_read_status(d["status"]) == ep.EP_ERR_CAPACITY
+    ref = oracle.ll_dispatch(x_host, idx, E, 2, 0)
+    assert ref["rc"] == oracle.ERR_CAPACITY
+    assert np.array_equal(np_(d["combine_idx"]), ref["combine_idx"])
+    assert np.array_equal(np_(d["recv_count"]), ref["recv_count"])
+
+
+def test_ll_rejects_tokens_above_capacity():
+    w = synth.scaled(synth.WORKLOADS["tiny"], T_r=17)
+    x_dev, _, idx_dev, _, _, _ = inputs(w)
+    with pytest.raises(ep.EPError) as ei:
+        gpu_ll_dispatch(x_dev, idx_dev, w.E, 16, 0)
+    assert ei.value.code == ep.EP_ERR_INVALID_ARG
+
+
+def test_ll_bounded_wait_on_a_chunk_that_never_publishes():
+    """Host-made fault: the workspace's ticket counter is advanced by one,
+    so the CTA for the first chunk never exists and its look-back words are
+    never published.  The other CTAs' waits must give up after their bound
+    (EP_ERR_TIMEOUT / EP_ERR_STATE in the status word), the kernel must
+    finish, and after ep_clean_ll_buffer the same workspace works again."""
+    w = synth.scaled(synth.WORKLOADS["decode"], T_r=128, H=128, fp8_mode=0)
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E)
+    ws[:4].view(torch.int32)[0] = 1            # ticket counter := 1
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, 0, ws=ws)
+    torch.cuda.synchronize()
+    code = ep.ep_read_status(d["status"])
+    assert code in (ep.EP_ERR_TIMEOUT, ep.EP_ERR_STATE)
+    ep.ep_clean_ll_buffer(d["recv_count"], w.R, w.E, ws)
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, 0, ws=ws)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_ll(w, x_host, idx, d, w.max_tokens_per_rank, 0)
+
+
+def test_clean_ll_buffer_zeroes_counts_and_workspace():
+    w = synth.WORKLOADS["tiny"]
+    x_dev, _, idx_dev, _, _, _ = inputs(w)
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, 0)
+    assert int(d["recv_count"].sum()) == w.T * w.k
+    ep.ep_clean_ll_buffer(d["recv_count"], w.R, w.E, d["ws"])
+    assert int(d["recv_count"].abs().sum()) == 0
+    assert int(d["ws"].sum()) == 0
