@@ -46,6 +46,12 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workloads", default="decode,prefill,skewed,large")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    # profiling aids (change the workload; never used for a reported number)
+    ap.add_argument("--tokens-per-rank", type=int, default=0,
+                    help="override T_r of every selected workload (profiling only)")
+    ap.add_argument("--no-combine", action="store_true",
+                    help="dispatch only, no expert-output buffer (profiling only)")
     return ap.parse_args(argv)
 
 
@@ -157,7 +163,7 @@ def alg_bytes(w, rows: int):
 class Runner:
     """Buffers and one step of one workload on the current GPU."""
 
-    def __init__(self, w, device):
+    def __init__(self, w, device, with_combine=True):
         import numpy as np
         import torch
 
@@ -172,11 +178,13 @@ class Runner:
         self.out = torch.empty_like(self.x)
         self.rows = int((idx >= 0).sum())
         self.ll = w.mode == "ll"
+        self.with_combine = with_combine
         if self.ll:
             self.buf = ep.alloc_ll(w.R, w.T_r, w.H, w.E, w.k, w.max_tokens_per_rank, w.fp8_mode,
                                    device=device)
             S = w.R * w.max_tokens_per_rank
-            self.y = synth.expert_outputs_torch(w.E * S, w.H, device).view(w.R, w.E_l, S, w.H)
+            if with_combine:
+                self.y = synth.expert_outputs_torch(w.E * S, w.H, device).view(w.R, w.E_l, S, w.H)
         else:
             self.lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E, device=device)
             self.nt = ep.alloc_notify(w.R, w.E, device=device)
@@ -187,7 +195,9 @@ class Runner:
                 self._layout_notify()
                 self.cap = int(self.host_rows.max())
             self.buf = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, self.cap, device=device)
-            self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(w.R, self.cap, w.H)
+            if with_combine:
+                self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(
+                    w.R, self.cap, w.H)
         torch.cuda.synchronize()
 
     def _layout_notify(self):
@@ -215,8 +225,9 @@ class Runner:
             if ev:
                 ev[1].record()
                 ev[2].record()
-            ep.ep_ll_combine(self.y, self.wts, b["combine_idx"], w.E, w.max_tokens_per_rank,
-                             self.out, self.status)
+            if self.with_combine:
+                ep.ep_ll_combine(self.y, self.wts, b["combine_idx"], w.E, w.max_tokens_per_rank,
+                                 self.out, self.status)
             if ev:
                 ev[3].record()
         else:
@@ -229,7 +240,8 @@ class Runner:
             if ev:
                 ev[1].record()
                 ev[2].record()
-            ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
+            if self.with_combine:
+                ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
             if ev:
                 ev[3].record()
 
@@ -439,18 +451,22 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     peak, peak_kind = peaks()
     names = [n.strip() for n in args.workloads.split(",") if n.strip()]
-    if HEADLINE not in names:
-        names.insert(0, HEADLINE)
+    head = names[0]
     results = {}
     clocks = None
     for name in names:
         w = synth.WORKLOADS[name]
-        runner = Runner(w, dev)
-        sampler = ClockSampler(local_rank) if name == HEADLINE else None
+        if args.tokens_per_rank > 0:
+            w = synth.scaled(w, T_r=args.tokens_per_rank,
+                             max_tokens_per_rank=max(w.max_tokens_per_rank, args.tokens_per_rank),
+                             num_worst_tokens=(w.R * args.tokens_per_rank
+                                               if w.num_worst_tokens >= 0 else -1))
+        runner = Runner(w, dev, with_combine=not args.no_combine)
+        sampler = ClockSampler(local_rank) if name == head else None
         if sampler:
             sampler.start()
         res = measure(runner, args.steps, args.warmup, world, flush,
-                      e2e=(name == HEADLINE and not args.no_e2e))
+                      e2e=(name == head and not args.no_e2e and not args.no_combine))
         if sampler:
             clocks = sampler.stop()
         res["step_ms_max"] = max_over_ranks(res["step_ms"], world)
@@ -460,11 +476,11 @@ def run_ours(args, rank, world, local_rank):
         res["combine_gbs"] = cbytes / (res["combine_ms"] * 1e-3) / 1e9
         res["tokens"] = w.T
         results[name] = (w, runner, res)
-        if name != HEADLINE:
+        if name != head:
             del runner
             torch.cuda.empty_cache()
 
-    w, runner, res = results[HEADLINE]
+    w, runner, res = results[head]
     ms = res["step_ms_max"]
     value = world * w.T / (ms * 1e-3)
     e2e = None
@@ -475,6 +491,8 @@ def run_ours(args, rank, world, local_rank):
                "d2h_bytes_per_step": res["e2e"]["d2h_bytes_per_step"], "ms_per_step": e2e_ms}
     # dominant kernel of the headline step: the one with the larger time
     dom = "combine" if res["combine_ms"] >= res["dispatch_ms"] else "dispatch"
+    if args.no_combine:
+        dom = "dispatch"
     kern = {"combine": "k_combine", "dispatch": "k_scatter"}[dom]
     src = os.path.join(ROOT, "combine_get_dispatch_gb300", "csrc",
                        "combine.cu" if dom == "combine" else "dispatch.cu")
@@ -483,14 +501,16 @@ def run_ours(args, rank, world, local_rank):
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_source": f"{peak_kind} hbm_gbs",
                 "alg_bytes_per_launch": res[f"{dom}_alg_bytes"],
-                "traffic": load_traffic(kern, HEADLINE, src)}
+                "traffic": load_traffic(kern, head, src)}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": workload_desc(w), "l2": "flushed before every step (512 MiB write)",
                        "parallelism": f"{world} replica(s), {w.R} ranks emulated per GPU",
-                       "data_types": "x bf16 -> E4M3+ue8m0 dispatch; y bf16 -> bf16 combine, fp32 accumulate"},
+                       "data_types": ("x bf16 -> " + {0: "bf16", 1: "E4M3 + fp32 scales",
+                                                         2: "E4M3 + ue8m0 scales"}[w.fp8_mode]
+                                      + " dispatch; y bf16 -> bf16 combine, fp32 accumulate")},
             "hbm_gbs": {"dispatch": round(res["dispatch_gbs"], 1),
                         "combine": round(res["combine_gbs"], 1),
                         "dispatch_frac": round(res["dispatch_gbs"] / peak, 4),
@@ -499,7 +519,7 @@ def run_ours(args, rank, world, local_rank):
             "roofline": roofline}
     others = {}
     for name, (wo, _, r) in results.items():
-        if name == HEADLINE:
+        if name == head:
             continue
         others[name] = {
             "workload": workload_desc(wo), "tokens_per_s": wo.T / (r["step_ms_max"] * 1e-3),
@@ -514,7 +534,7 @@ def run_ours(args, rank, world, local_rank):
     line["kernels_ms"] = {"dispatch": round(res["dispatch_ms"], 5),
                           "combine": round(res["combine_ms"], 5)}
     if rank == 0:
-        if world == 1:
+        if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
     return 0
