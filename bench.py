@@ -174,7 +174,7 @@ class Runner:
         self.wts = torch.from_numpy(wts).to(device)
         self.x = synth.activations_torch(w, device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, device=device)
+        self.ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H, device=device)
         self.out = torch.empty_like(self.x)
         self.rows = int((idx >= 0).sum())
         self.ll = w.mode == "ll"
@@ -236,7 +236,8 @@ class Runner:
                 ev[0].record()
             ep.ep_dispatch(self.x, self.idx, self.lay["slot_rank"], self.nt["expert_prefix"],
                            self.nt["psum"], w.E, w.fp8_mode, self.cap, b["recv_x"],
-                           b["recv_scales"], b["recv_src_idx"], b["combine_idx"], self.status)
+                           b["recv_scales"], b["recv_src_idx"], b["combine_idx"], self.ws,
+                           self.status)
             if ev:
                 ev[1].record()
                 ev[2].record()

@@ -3,195 +3,399 @@
 // §3.2, §4.3).
 //
 // Every emulated rank's receive buffer is a partition of this GPU's HBM, so
-// the "put" of a token to expert e's rank is a plain store into that
-// partition.  One warp handles one (token, 1024-channel segment) item: it
-// reads the segment of x once with 16-byte streaming loads (512 contiguous
-// bytes per warp instruction), quantises it once when FP8 is requested
-// (amax over each 128-channel block by a 16-lane shuffle reduction), and
-// stores it to the k destination rows.  The destinations come from
+// the "put" of a token to expert e's rank is a store into that partition.
+// The scatter is built on TMA bulk copies (cp.async.bulk): every warp runs
+// its own pipeline over (token, row piece) units --
+//   * lane 0 streams the source pieces global -> shared with bulk copies
+//     that complete on per-stage mbarriers, units ahead of the one being
+//     consumed (deep memory-level parallelism from one thread);
+//   * bf16: the staged piece is written to its k destination rows straight
+//     from shared memory by k bulk stores (no register traffic at all);
+//   * FP8: the 32 lanes quantise the staged piece once (each lane owns 16
+//     channels, a 128-channel scale block is 8 lanes, amax by a 3-step
+//     shuffle reduction) into a staged E4M3 piece, which k bulk stores write.
+// The destinations come from
 //   normal mode:       psum[r][l] + expert_prefix[i][e] + slot_rank[i][t][j]
 //                      (segment start + source-rank offset + position, the
-//                      receiver address of §2.3 with V2's psum, §4.3)
+//                      receiver address of §2.3 with V2's psum of §4.3)
 //   low-latency mode:  combine_idx written by the layout kernel just before
-//                      (packed row in (rank, token, slot) order, §1.2/§3.2).
-// The low-latency scatter is a programmatic dependent launch: it loads its
-// first segment of x while the layout kernel is still running and only then
-// waits for the layout (griddepcontrol.wait).
+//                      (packed row in (rank, token, slot) order, §1.2/§3.2)
+// and are fetched one / two units ahead of their use.  The low-latency
+// scatter is a programmatic dependent launch of the layout kernel: its first
+// bulk loads of x are issued before it waits for the layout.
+//
+// Scales.  The receive layout keeps them column-major ([segment][block][row],
+// §1.2): one value per row and block at a stride of a whole column.  Stored
+// from the token side that is one scattered 1- or 4-byte store per
+// (destination row, block) -- measured ~20% of the FP8 dispatch time.  So
+// the scatter writes each token's scales once, row-major, into the
+// workspace, and k_scale_columns (a programmatic dependent of the scatter)
+// gathers them into the column layout with stores coalesced along rows.
 //
 // FP8 arithmetic is exact IEEE: amax is floored at 1e-4, the scale and its
 // inverse use correctly rounded division (__fdiv_rn), x * inv one rounded
 // multiply (__fmul_rn), and the E4M3 conversion is CUDA's satfinite RNE
 // intrinsic; ue8m0 scales are amax/448 rounded up to a power of two through
 // the exponent bits, so x * 2^-p is exact.
+//
+// Every mbarrier wait is bounded (kWaitNs); on expiry the warp records
+// EP_ERR_TIMEOUT, stops issuing work, waits (bounded) for its copies in
+// flight and leaves.
 
 #include "ep_common.cuh"
 #include "layout.cuh"
 
 namespace ep {
 
-constexpr int kScatterThreads = 256;
-constexpr int kScatterU = 4;                          // 16-byte vectors per lane per item
-constexpr int kScatterSegC = kScatterU * kWarp * 8;   // 1024 channels per item
+constexpr int kScatterMaxWarps = 16;
+constexpr int kBf16Warps = 8;      // target warps per CTA, bf16 path
+constexpr int kFp8Warps = 16;      // target warps per CTA, FP8 path
+constexpr int kBf16Stages = 3;     // staged source pieces per warp (bf16 path)
+constexpr int kFp8InStages = 2;    // staged source pieces per warp (FP8 path)
+constexpr int kFp8OutStages = 2;   // staged E4M3 pieces per warp
+constexpr size_t kScatterSmemBudget = 200 * 1024;
 constexpr int kPadChunkRows = 1024;
+constexpr int kScaleColThreads = 256;
 
 struct ScatterParams {
   const uint8_t* x;
   int R, T_r, H, E, E_l, k;
   int64_t T;
-  int nseg;
   const int64_t* topk_idx;
   const int32_t* slot_rank;
   const int32_t* expert_prefix;
   const int64_t* psum;
-  int64_t seg_rows;
+  int64_t seg_rows;        // rows per segment (cap_rows, or R*max per expert)
   int64_t n_rows;          // rows of the whole receive buffer
   uint8_t* recv_x;
-  void* recv_scales;
   int32_t* recv_src_idx;
   int32_t* combine_idx;
+  uint8_t* scale_rows;     // [T][scale_row_bytes] per-token scales (FP8)
+  int scale_row_bytes;
   int32_t* status;
-  int64_t n_items;
+  // pipeline geometry
+  int Hp;                  // channels per row piece
+  int P;                   // pieces per row
+  int warps_per_cta;
+  uint32_t warp_smem;      // bytes of shared memory per warp
+  uint32_t in_bytes, out_bytes;   // per-stage sizes (128-byte multiples)
+  int64_t n_units;         // T * P
   int64_t n_pad_items;
   int tail_chunks;
 };
 
-// Quantise 8 channels held by this lane; amax is reduced over the 16 lanes
-// that share the 128-channel block.  Returns the 8 E4M3 bytes; the block's
-// scale goes to *scale_f32 / *scale_u8.
+__host__ __device__ inline uint32_t round128(uint32_t v) { return (v + 127u) / 128u * 128u; }
+
+// Bytes of one token's staged scales (16-byte rows).
+__host__ __device__ inline int scale_row_bytes(int H, int elem) {
+  return ((H / kFp8Block) * elem + 15) / 16 * 16;
+}
+
+// Quantise 16 channels (two 16-byte bf16 vectors) of this lane; amax is
+// reduced over the 8 lanes sharing the 128-channel block.  Returns 16 E4M3
+// bytes; the block's scale goes to *sf (fp32 mode) or *su (ue8m0 mode).
 template <int kMode>
-__device__ __forceinline__ uint2 quantize8(const uint4 v, float* scale_f32, uint32_t* scale_u8) {
-  float f[8];
-  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+__device__ __forceinline__ uint4 quantize16(const uint4 a, const uint4 b, float* sf, uint32_t* su) {
+  float f[16];
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    f[2 * c] = bf16_lo(w[c]);
+    f[2 * c + 1] = bf16_hi(w[c]);
+  }
   float amax = 0.0f;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) amax = fmaxf(amax, fabsf(f[c]));
+  for (int c = 0; c < 16; ++c) amax = fmaxf(amax, fabsf(f[c]));
 #pragma unroll
-  for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  for (int off = 4; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   amax = fmaxf(amax, 1e-4f);
   float mul;
   if (kMode == EP_FP8_E4M3_F32_SCALE) {
-    *scale_f32 = __fdiv_rn(amax, 448.0f);
+    *sf = __fdiv_rn(amax, 448.0f);
     mul = __fdiv_rn(448.0f, amax);
   } else {
     const uint32_t bits = __float_as_uint(__fdiv_rn(amax, 448.0f));
     uint32_t biased = (bits >> 23) & 0xffu;
     if (bits & 0x7fffffu) biased += 1u;
-    *scale_u8 = biased;
+    *su = biased;
     mul = __uint_as_float((254u - biased) << 23);   // 2^(127 - biased), exact
   }
-  uint2 q;
-  q.x = cvt_e4m3x2(__fmul_rn(f[0], mul), __fmul_rn(f[1], mul)) |
-        (cvt_e4m3x2(__fmul_rn(f[2], mul), __fmul_rn(f[3], mul)) << 16);
-  q.y = cvt_e4m3x2(__fmul_rn(f[4], mul), __fmul_rn(f[5], mul)) |
-        (cvt_e4m3x2(__fmul_rn(f[6], mul), __fmul_rn(f[7], mul)) << 16);
-  return q;
+  uint32_t q[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    q[c] = cvt_e4m3x2(__fmul_rn(f[4 * c], mul), __fmul_rn(f[4 * c + 1], mul)) |
+           (cvt_e4m3x2(__fmul_rn(f[4 * c + 2], mul), __fmul_rn(f[4 * c + 3], mul)) << 16);
+  }
+  return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
-template <int kMode, bool kLL>
-__global__ void __launch_bounds__(kScatterThreads, 4) k_scatter(ScatterParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = ((int64_t)blockIdx.x * kScatterThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kScatterThreads) >> 5;
-  const int nb = p.H / kFp8Block;
-  const int64_t row_bytes = kMode == EP_FP8_NONE ? (int64_t)p.H * 2 : (int64_t)p.H;
-  bool waited = false;
+// ------------------------------------------------------------------ warp pipeline
 
-  for (int64_t it = warp0; it < p.n_items; it += nwarps) {
-    const int64_t g = it / p.nseg;
-    const int s = (int)(it - g * p.nseg);
-    const int ch0 = s * kScatterSegC;
-    const uint8_t* xrow = p.x + g * (int64_t)p.H * 2;
+// One warp's TMA pipeline over its units u = first + i * stride (i < count);
+// unit u is piece u % P of token u / P.  Units are walked with incremental
+// (token, piece) cursors, so the loop does no integer division.
+struct Pipe {
+  uint8_t* s_in;            // [NS][in_bytes] staged bf16 source pieces
+  uint8_t* s_out;           // [NO][out_bytes] staged E4M3 pieces
+  uint64_t* bar;            // [NS] mbarriers of the source stages
+  uint32_t in_bytes, out_bytes;
+  int H, Hp, P, k;
+  const uint8_t* x;
+  uint8_t* recv_x;
+  uint8_t* scale_rows;
+  int scale_row_bytes;
+  int32_t* status;
+  int32_t first, stride, count;
+  int32_t stride_g, stride_pc;   // stride / P, stride % P
+};
 
-    uint4 v[kScatterU];
-#pragma unroll
-    for (int u = 0; u < kScatterU; ++u) {
-      const int ch = ch0 + u * 256 + lane * 8;
-      v[u] = ch < p.H ? ld_stream_v4(xrow + (int64_t)ch * 2) : make_uint4(0, 0, 0, 0);
+struct Cursor {
+  int32_t g, pc;
+};
+
+__device__ __forceinline__ Cursor cursor_at(const Pipe& q, int32_t u) {
+  Cursor c;
+  c.g = u / q.P;
+  c.pc = u - c.g * q.P;
+  return c;
+}
+
+__device__ __forceinline__ void cursor_next(const Pipe& q, Cursor& c) {
+  c.g += q.stride_g;
+  c.pc += q.stride_pc;
+  if (c.pc >= q.P) {
+    c.pc -= q.P;
+    c.g += 1;
+  }
+}
+
+template <int kMode>
+struct PipeDepth {
+  static constexpr bool kFp8 = kMode != EP_FP8_NONE;
+  static constexpr int NS = kFp8 ? kFp8InStages : kBf16Stages;
+  static constexpr int NO = kFp8 ? kFp8OutStages : 1;
+  static constexpr int kPrologue = kFp8 ? NS : NS - 1;   // loads issued before the loop
+};
+
+// Lane 0: bulk-load unit i (at cursor c) into stage i % NS.
+template <int kMode>
+__device__ __forceinline__ void pipe_issue_load(const Pipe& q, int32_t i, const Cursor& c) {
+  constexpr int NS = PipeDepth<kMode>::NS;
+  const uint32_t bytes = (uint32_t)min(q.Hp, q.H - c.pc * q.Hp) * 2u;
+  uint64_t* b = &q.bar[i % NS];
+  mbar_arrive_expect_tx(b, bytes);
+  tma_load_1d(q.s_in + (size_t)(i % NS) * q.in_bytes,
+              q.x + (int64_t)c.g * q.H * 2 + (int64_t)c.pc * q.Hp * 2, bytes, b);
+}
+
+// Barrier set-up and the first source loads (they depend on nothing but x).
+// Returns the cursor of the next unit to load.
+template <int kMode>
+__device__ __forceinline__ Cursor pipe_prologue(const Pipe& q, int lane) {
+  Cursor c = cursor_at(q, q.first);
+  if (q.count <= 0) return c;
+  const int32_t pro = min((int32_t)PipeDepth<kMode>::kPrologue, q.count);
+  if (lane == 0) {
+    for (int s = 0; s < PipeDepth<kMode>::NS; ++s) mbar_init(&q.bar[s], 1);
+    fence_barrier_init();
+  }
+  for (int32_t i = 0; i < pro; ++i) {
+    if (lane == 0) pipe_issue_load<kMode>(q, i, c);
+    cursor_next(q, c);
+  }
+  __syncwarp();
+  return c;
+}
+
+// Run the pipeline.  D supplies each unit's destinations in two stages so
+// that their global loads are issued one / two units ahead of their use:
+//   d.pre(g, lane)              first-level value for slot lane (lane < k)
+//   d.fin(g, pc, lane, pre)     flat receive row of slot lane, or -1
+template <int kMode, class D>
+__device__ __forceinline__ void pipe_run(const Pipe& q, const D& d, int lane, Cursor ld) {
+  constexpr bool kFp8 = PipeDepth<kMode>::kFp8;
+  constexpr int NS = PipeDepth<kMode>::NS;
+  constexpr int NO = PipeDepth<kMode>::NO;
+  constexpr int kEs = kMode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
+  const int32_t n = q.count;
+  if (n <= 0) return;
+  const int64_t row_bytes = kFp8 ? (int64_t)q.H : (int64_t)q.H * 2;
+  Cursor cur = cursor_at(q, q.first);
+  Cursor c1 = cur, c2 = cur;
+  cursor_next(q, c1);
+  cursor_next(q, c2);
+  cursor_next(q, c2);
+  int64_t pre_a = d.pre(cur.g, lane);
+  int64_t pre_b = n > 1 ? d.pre(c1.g, lane) : -1;
+  int32_t ld_i = min((int32_t)PipeDepth<kMode>::kPrologue, n);   // next unit to load
+
+  bool failed = false;
+  int32_t i = 0;
+  for (; i < n; ++i) {
+    const int hc = min(q.Hp, q.H - cur.pc * q.Hp);
+    const int s = i % NS;
+    const int32_t my_f = d.fin(cur.g, cur.pc, lane, pre_a);
+    pre_a = pre_b;
+    if (i + 2 < n) pre_b = d.pre(c2.g, lane);
+    const bool landed = mbar_wait_bounded(&q.bar[s], (uint32_t)((i / NS) & 1));
+    if (!__all_sync(0xffffffffu, landed)) {   // warp-uniform decision
+      set_status(q.status, EP_ERR_TIMEOUT);
+      failed = true;
+      break;
     }
-    if (kLL && !waited) {
-      pdl_wait();
-      waited = true;
-    }
-
-    // destination of slot j = lane (flat row, scale base)
-    int64_t my_f = -1, my_sb = 0;
-    if (lane < p.k) {
-      const int64_t pos = g * p.k + lane;
-      if (kLL) {
-        my_f = p.combine_idx[pos];
-        if (my_f < -1 || my_f >= p.n_rows) {   // never write outside the buffer
-          set_status(p.status, EP_ERR_INVALID_ARG);
-          my_f = -1;
-        }
-      } else {
-        const int64_t e = p.topk_idx[pos];
-        if (e >= 0 && e < p.E) {
-          const int r = (int)(e / p.E_l);
-          const int l = (int)(e - (int64_t)r * p.E_l);
-          const int i = (int)(g / p.T_r);
-          const int64_t row = p.psum[(int64_t)r * (p.E_l + 1) + l] +
-                              p.expert_prefix[(int64_t)i * p.E + e] + p.slot_rank[pos];
-          if (row >= 0 && row < p.seg_rows) my_f = (int64_t)r * p.seg_rows + row;
-          else set_status(p.status, EP_ERR_CAPACITY);
-        } else if (e != -1) {
-          set_status(p.status, EP_ERR_INVALID_ARG);
-        }
-        if (s == 0) {
-          p.combine_idx[pos] = (int32_t)my_f;
-          if (my_f >= 0) p.recv_src_idx[my_f] = (int32_t)g;
-        }
+    const int64_t col = (int64_t)cur.pc * q.Hp * (kFp8 ? 1 : 2);   // byte offset of the piece
+    if (!kFp8) {
+      const uint8_t* src = q.s_in + (size_t)s * q.in_bytes;
+      for (int j = 0; j < q.k; ++j) {
+        const int32_t f = __shfl_sync(0xffffffffu, my_f, j);
+        if (lane == 0 && f >= 0) tma_store_1d(q.recv_x + f * row_bytes + col, src, (uint32_t)hc * 2u);
       }
-      if (my_f >= 0 && kMode != EP_FP8_NONE) {
-        const int64_t seg = my_f / p.seg_rows;
-        my_sb = seg * nb * p.seg_rows + (my_f - seg * p.seg_rows);
+      // unit i-1's stores have read their stage: refill it with unit i+NS-1
+      if (lane == 0) {
+        tma_commit();
+        tma_wait_read<1>();
+        if (ld_i < n) pipe_issue_load<kMode>(q, ld_i, ld);
       }
-    }
-
-    if (kMode == EP_FP8_NONE) {
-      for (int j = 0; j < p.k; ++j) {
-        const int64_t f = __shfl_sync(0xffffffffu, my_f, j);
-        if (f < 0) continue;
-        uint8_t* dst = p.recv_x + f * row_bytes;
-#pragma unroll
-        for (int u = 0; u < kScatterU; ++u) {
-          const int ch = ch0 + u * 256 + lane * 8;
-          if (ch < p.H) st_v4(dst + (int64_t)ch * 2, v[u]);
-        }
+      if (ld_i < n) {
+        ++ld_i;
+        cursor_next(q, ld);
       }
+      __syncwarp();
     } else {
-      uint2 q[kScatterU];
-      float sf[kScatterU];
-      uint32_t su[kScatterU];
-#pragma unroll
-      for (int u = 0; u < kScatterU; ++u) q[u] = quantize8<kMode>(v[u], &sf[u], &su[u]);
-      for (int j = 0; j < p.k; ++j) {
-        const int64_t f = __shfl_sync(0xffffffffu, my_f, j);
-        if (f < 0) continue;
-        const int64_t sb = __shfl_sync(0xffffffffu, my_sb, j);
-        uint8_t* dst = p.recv_x + f * row_bytes;
-#pragma unroll
-        for (int u = 0; u < kScatterU; ++u) {
-          const int ch = ch0 + u * 256 + lane * 8;
-          if (ch < p.H) {
-            st_v2(dst + ch, q[u]);
-            if ((lane & 15) == 0) {
-              const int64_t sidx = sb + (int64_t)(ch / kFp8Block) * p.seg_rows;
-              if (kMode == EP_FP8_E4M3_F32_SCALE)
-                static_cast<float*>(p.recv_scales)[sidx] = sf[u];
-              else
-                static_cast<uint8_t*>(p.recv_scales)[sidx] = (uint8_t)su[u];
-            }
+      const int o = i % NO;
+      if (lane == 0 && i >= NO) tma_wait_read<NO - 1>();   // out stage o is free again
+      __syncwarp();
+      const uint8_t* src = q.s_in + (size_t)s * q.in_bytes;
+      uint8_t* dst = q.s_out + (size_t)o * q.out_bytes;
+      uint8_t* srow = q.scale_rows + (int64_t)cur.g * q.scale_row_bytes;
+      for (int c0 = lane * 16; c0 < ((hc + 511) / 512) * 512; c0 += 512) {
+        const bool ok = c0 < hc;
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
+        if (ok) {
+          a = ld_shared_v4(src + (size_t)c0 * 2);
+          b = ld_shared_v4(src + (size_t)c0 * 2 + 16);
+        }
+        float sf;
+        uint32_t su;
+        const uint4 qv = quantize16<kMode>(a, b, &sf, &su);
+        if (ok) {
+          st_shared_v4(dst + c0, qv);
+          if ((lane & 7) == 0) {   // the token's scale of this block, row-major staging
+            const int blk = (cur.pc * q.Hp + c0) >> 7;
+            if (kEs == 4) reinterpret_cast<float*>(srow)[blk] = sf;
+            else srow[blk] = (uint8_t)su;
           }
         }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      // source stage s was fully read: refill it with unit i+NS
+      if (lane == 0 && ld_i < n) pipe_issue_load<kMode>(q, ld_i, ld);
+      if (ld_i < n) {
+        ++ld_i;
+        cursor_next(q, ld);
+      }
+      for (int j = 0; j < q.k; ++j) {
+        const int32_t f = __shfl_sync(0xffffffffu, my_f, j);
+        if (lane == 0 && f >= 0) tma_store_1d(q.recv_x + f * row_bytes + col, dst, (uint32_t)hc);
+      }
+      if (lane == 0) tma_commit();
     }
+    cur = c1;
+    c1 = c2;
+    cursor_next(q, c2);
   }
+  if (failed && lane == 0) {
+    // drain (bounded) the loads this warp still has in flight
+    for (int32_t r = i; r < ld_i; ++r) mbar_wait_bounded(&q.bar[r % NS], (uint32_t)((r / NS) & 1));
+  }
+  if (lane == 0) tma_wait_all();
+}
 
-  if (kLL) return;
-  // normal mode: recv_src_idx = -1 on alignment padding and past the last row
+// Carve this warp's pipeline out of the CTA's shared memory; units
+// first, first + stride, ... (count of them).
+template <int kMode>
+__device__ __forceinline__ Pipe make_pipe(uint8_t* smem, const ScatterParams& p, int warp,
+                                          int32_t first, int32_t stride, int32_t count) {
+  Pipe q;
+  uint8_t* ws = smem + (size_t)warp * p.warp_smem;
+  q.s_in = ws;
+  q.s_out = q.s_in + (size_t)PipeDepth<kMode>::NS * p.in_bytes;
+  q.bar = reinterpret_cast<uint64_t*>(q.s_out + (size_t)PipeDepth<kMode>::NO * p.out_bytes);
+  q.in_bytes = p.in_bytes;
+  q.out_bytes = p.out_bytes;
+  q.H = p.H;
+  q.Hp = p.Hp;
+  q.P = p.P;
+  q.k = p.k;
+  q.x = p.x;
+  q.recv_x = p.recv_x;
+  q.scale_rows = p.scale_rows;
+  q.scale_row_bytes = p.scale_row_bytes;
+  q.status = p.status;
+  q.first = first;
+  q.stride = stride;
+  q.count = count;
+  q.stride_g = stride / p.P;
+  q.stride_pc = stride - q.stride_g * p.P;
+  return q;
+}
+
+// ------------------------------------------------------------------ destinations
+
+// Normal mode: e = topk_idx (first level), then segment start + source-rank
+// offset + slot rank (second level); records combine_idx / recv_src_idx on
+// the token's first piece.
+struct NormalDest {
+  const ScatterParams* p;
+  __device__ __forceinline__ int64_t pre(int32_t g, int lane) const {
+    return lane < p->k ? __ldg(&p->topk_idx[(int64_t)g * p->k + lane]) : -1;
+  }
+  __device__ __forceinline__ int32_t fin(int32_t g, int pc, int lane, int64_t e64) const {
+    if (lane >= p->k) return -1;
+    const int64_t pos = (int64_t)g * p->k + lane;
+    int32_t f = -1;
+    if (e64 >= 0 && e64 < p->E) {
+      const int e = (int)e64;
+      const int r = e / p->E_l;
+      const int l = e - r * p->E_l;
+      const int i = g / p->T_r;
+      const int64_t row = __ldg(&p->psum[(int64_t)r * (p->E_l + 1) + l]) +
+                          __ldg(&p->expert_prefix[(int64_t)i * p->E + e]) + __ldg(&p->slot_rank[pos]);
+      if (row >= 0 && row < p->seg_rows) f = (int32_t)((int64_t)r * p->seg_rows + row);
+      else set_status(p->status, EP_ERR_CAPACITY);
+    } else if (e64 != -1) {
+      set_status(p->status, EP_ERR_INVALID_ARG);
+    }
+    if (pc == 0) {
+      p->combine_idx[pos] = f;
+      if (f >= 0) p->recv_src_idx[f] = g;
+    }
+    return f;
+  }
+};
+
+// Low-latency mode after the layout kernel: the packed row is combine_idx.
+struct PackedDest {
+  const ScatterParams* p;
+  __device__ __forceinline__ int64_t pre(int32_t g, int lane) const {
+    return lane < p->k ? (int64_t)p->combine_idx[(int64_t)g * p->k + lane] : -1;
+  }
+  __device__ __forceinline__ int32_t fin(int32_t, int, int lane, int64_t f) const {
+    if (lane >= p->k) return -1;
+    if (f < -1 || f >= p->n_rows) {   // never write outside the buffer
+      set_status(p->status, EP_ERR_INVALID_ARG);
+      return -1;
+    }
+    return (int32_t)f;
+  }
+};
+
+// Normal mode: recv_src_idx = -1 on alignment padding and past the last row
+// of every rank (work items spread over the warps gw, gw + W, ...).
+__device__ __forceinline__ void pad_fill(const ScatterParams& p, int32_t gw, int32_t W, int lane) {
   const int n_seg_items = p.R * p.E_l;
-  for (int64_t it = warp0; it < p.n_pad_items; it += nwarps) {
+  for (int64_t it = gw; it < p.n_pad_items; it += W) {
     int r;
     int64_t lo, hi;
     if (it < n_seg_items) {
@@ -201,9 +405,9 @@ __global__ void __launch_bounds__(kScatterThreads, 4) k_scatter(ScatterParams p)
       lo = p.psum[(int64_t)r * (p.E_l + 1) + l] + p.expert_prefix[(int64_t)p.R * p.E + e];
       hi = p.psum[(int64_t)r * (p.E_l + 1) + l + 1];
     } else {
-      const int64_t q = it - n_seg_items;
-      r = (int)(q / p.tail_chunks);
-      const int64_t c = q - (int64_t)r * p.tail_chunks;
+      const int64_t c4 = it - n_seg_items;
+      r = (int)(c4 / p.tail_chunks);
+      const int64_t c = c4 - (int64_t)r * p.tail_chunks;
       lo = max(p.psum[(int64_t)r * (p.E_l + 1) + p.E_l], c * kPadChunkRows);
       hi = (c + 1) * kPadChunkRows;
     }
@@ -214,14 +418,380 @@ __global__ void __launch_bounds__(kScatterThreads, 4) k_scatter(ScatterParams p)
 }
 
 template <int kMode, bool kLL>
-static int launch_scatter_t(const ScatterParams& p, cudaStream_t stream, bool pdl) {
-  const int64_t total = p.n_items + p.n_pad_items;
-  const int64_t want = (total + (kScatterThreads / kWarp) - 1) / (kScatterThreads / kWarp);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::num_sms() * 4));
+__global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  if (kMode != EP_FP8_NONE) pdl_launch_dependents();   // the scale-column pass may launch
+  const int32_t gw = blockIdx.x * p.warps_per_cta + warp;
+  const int32_t W = gridDim.x * p.warps_per_cta;
+  const int32_t n_units = (int32_t)p.n_units;
+  const int32_t count = gw < n_units ? (n_units - gw + W - 1) / W : 0;
+  Pipe q = make_pipe<kMode>(smem, p, warp, gw, W, count);
+  const Cursor ld = pipe_prologue<kMode>(q, lane);
+  if (kLL) {
+    pdl_wait();   // combine_idx of the layout kernel is read from here on
+    pipe_run<kMode>(q, PackedDest{&p}, lane, ld);
+    return;
+  }
+  pipe_run<kMode>(q, NormalDest{&p}, lane, ld);
+  pad_fill(p, gw, W, lane);
+}
+
+// ------------------------------------------------------------------ staged low latency
+
+constexpr int kStagedWarps = 16;
+constexpr int kStagedMaxPerWarp = 8;    // units per warp
+constexpr int kStagedPiece = 1024;      // channels per unit
+
+// Low-latency scatter of a batch whose source rows fit in the CTAs' shared
+// memory (decode sizes).  Everything that does not need the layout is done
+// while the layout kernel still runs: each warp bulk-loads ALL its units'
+// bf16 pieces at once, one slot and one mbarrier per unit, and (FP8)
+// quantises every piece in place (a lane reads its 32 bytes, the warp syncs,
+// then the lane writes its 16 E4M3 bytes over the front of the slot).  Only
+// then does it wait for the layout (griddepcontrol.wait), fetch all its
+// destinations at once and issue the bulk stores back to back, so the store
+// stream starts the moment the layout is known and never waits on a load.
+template <int kMode>
+__global__ void __launch_bounds__(kStagedWarps * kWarp, 1) k_ll_scatter_staged(ScatterParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr bool kFp8 = kMode != EP_FP8_NONE;
+  constexpr int kEs = kMode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  if (kFp8) pdl_launch_dependents();   // the scale-column pass may launch
+  const int32_t U = (int32_t)p.n_units;
+  const int32_t u0 = (int32_t)((int64_t)U * blockIdx.x / gridDim.x);
+  const int32_t u1 = (int32_t)((int64_t)U * (blockIdx.x + 1) / gridDim.x);
+  const int32_t nm = warp < u1 - u0 ? (u1 - u0 - warp + kStagedWarps - 1) / kStagedWarps : 0;
+  const uint32_t slot_bytes = p.in_bytes;   // one bf16 piece
+  uint8_t* slots = smem;                    // [units of this CTA][slot_bytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)p.warp_smem) + warp * kStagedMaxPerWarp;
+  const int64_t row_bytes = kFp8 ? (int64_t)p.H : (int64_t)p.H * 2;
+  auto unit_slot = [&](int32_t m) { return slots + (size_t)(warp + m * kStagedWarps) * slot_bytes; };
+  auto unit_of = [&](int32_t m, int32_t* g, int* pc) {
+    const int32_t u = u0 + warp + m * kStagedWarps;
+    *g = u / p.P;
+    *pc = u - *g * p.P;
+  };
+
+  // ---- 1. all source pieces in flight
+  if (nm > 0 && lane == 0) {
+    for (int32_t m = 0; m < nm; ++m) mbar_init(&bars[m], 1);
+    fence_barrier_init();
+    for (int32_t m = 0; m < nm; ++m) {
+      int32_t g;
+      int pc;
+      unit_of(m, &g, &pc);
+      const uint32_t bytes = (uint32_t)min(p.Hp, p.H - pc * p.Hp) * 2u;
+      mbar_arrive_expect_tx(&bars[m], bytes);
+      tma_load_1d(unit_slot(m), p.x + (int64_t)g * p.H * 2 + (int64_t)pc * p.Hp * 2, bytes, &bars[m]);
+    }
+  }
+  __syncwarp();
+  bool ok_all = true;
+  for (int32_t m = 0; m < nm; ++m) {
+    const bool landed = mbar_wait_bounded(&bars[m], 0);
+    if (!__all_sync(0xffffffffu, landed)) {
+      set_status(p.status, EP_ERR_TIMEOUT);
+      ok_all = false;
+      if (lane == 0)   // wait (bounded) for what is still in flight
+        for (int32_t r = m; r < nm; ++r) mbar_wait_bounded(&bars[r], 0);
+      break;
+    }
+    if (kFp8) {   // ---- 2. quantise in place
+      int32_t g;
+      int pc;
+      unit_of(m, &g, &pc);
+      const int hc = min(p.Hp, p.H - pc * p.Hp);
+      uint8_t* sl = unit_slot(m);
+      uint8_t* srow = p.scale_rows + (int64_t)g * p.scale_row_bytes;
+      constexpr int kSegs = kStagedPiece / 512;
+      uint4 a[kSegs], b[kSegs];
+#pragma unroll
+      for (int sg = 0; sg < kSegs; ++sg) {
+        const int c0 = sg * 512 + lane * 16;
+        a[sg] = make_uint4(0, 0, 0, 0);
+        b[sg] = a[sg];
+        if (c0 < hc) {
+          a[sg] = ld_shared_v4(sl + (size_t)c0 * 2);
+          b[sg] = ld_shared_v4(sl + (size_t)c0 * 2 + 16);
+        }
+      }
+      __syncwarp();   // every lane has read its bf16 before any E4M3 lands on top
+#pragma unroll
+      for (int sg = 0; sg < kSegs; ++sg) {
+        const int c0 = sg * 512 + lane * 16;
+        float sf;
+        uint32_t su;
+        const uint4 qv = quantize16<kMode>(a[sg], b[sg], &sf, &su);
+        if (c0 < hc) {
+          st_shared_v4(sl + c0, qv);
+          if ((lane & 7) == 0) {
+            const int blk = (pc * p.Hp + c0) >> 7;
+            if (kEs == 4) reinterpret_cast<float*>(srow)[blk] = sf;
+            else srow[blk] = (uint8_t)su;
+          }
+        }
+      }
+    }
+  }
+  if (kFp8) fence_proxy_async_smem();
+  __syncwarp();
+
+  // ---- 3. the layout is needed from here on
+  pdl_wait();
+  int32_t fm[kStagedMaxPerWarp];
+#pragma unroll
+  for (int m = 0; m < kStagedMaxPerWarp; ++m) {
+    fm[m] = -1;
+    if (m < nm && lane < p.k) {
+      int32_t g;
+      int pc;
+      unit_of(m, &g, &pc);
+      int32_t f = p.combine_idx[(int64_t)g * p.k + lane];
+      if (f < -1 || (int64_t)f >= p.n_rows) {
+        set_status(p.status, EP_ERR_INVALID_ARG);
+        f = -1;
+      }
+      fm[m] = f;
+    }
+  }
+  if (ok_all) {
+#pragma unroll
+    for (int m = 0; m < kStagedMaxPerWarp; ++m) {
+      if (m < nm) {
+        int32_t g;
+        int pc;
+        unit_of(m, &g, &pc);
+        const int hc = min(p.Hp, p.H - pc * p.Hp);
+        const int64_t col = (int64_t)pc * p.Hp * (kFp8 ? 1 : 2);
+        const uint32_t bytes = (uint32_t)hc * (kFp8 ? 1u : 2u);
+        for (int j = 0; j < p.k; ++j) {
+          const int32_t f = __shfl_sync(0xffffffffu, fm[m], j);
+          if (lane == 0 && f >= 0) tma_store_1d(p.recv_x + f * row_bytes + col, unit_slot(m), bytes);
+        }
+      }
+    }
+  }
+  if (lane == 0 && nm > 0) {
+    tma_commit();
+    tma_wait_all();
+  }
+}
+
+// Geometry of the staged path, or false when the batch does not fit.
+static size_t staged_smem(const ScatterParams& p) {
+  return (size_t)p.warp_smem + (size_t)kStagedWarps * kStagedMaxPerWarp * sizeof(uint64_t);
+}
+
+static bool plan_staged(ScatterParams& p) {
+  const int hp = std::min(p.H, kStagedPiece);
+  p.Hp = hp;
+  p.P = (p.H + hp - 1) / hp;
+  p.n_units = p.T * p.P;
+  const int grid = ep_host::num_sms();
+  const int64_t per_cta = (p.n_units + grid - 1) / grid;
+  if (per_cta > (int64_t)kStagedWarps * kStagedMaxPerWarp) return false;
+  p.in_bytes = round128((uint32_t)hp * 2u);            // one slot per unit
+  p.warp_smem = (uint32_t)(per_cta * p.in_bytes);      // slot area of the CTA
+  p.warps_per_cta = kStagedWarps;
+  return staged_smem(p) <= kScatterSmemBudget;
+}
+
+template <int kMode>
+static int launch_ll_staged_t(ScatterParams p, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_ll_scatter_staged<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kScatterSmemBudget + 1024) != cudaSuccess) {
+      cudaGetLastError();
+      return EP_ERR_CUDA;
+    }
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ep_host::num_sms());
+  cfg.blockDim = dim3(kStagedWarps * kWarp);
+  cfg.dynamicSmemBytes = staged_smem(p);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_ll_scatter_staged<kMode>, p) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
+  ep_host::count_launch();
+  return ep_host::check_launch();
+}
+
+static int launch_ll_staged(const ScatterParams& p, int fp8_mode, cudaStream_t stream) {
+  switch (fp8_mode) {
+    case EP_FP8_NONE: return launch_ll_staged_t<EP_FP8_NONE>(p, stream);
+    case EP_FP8_E4M3_F32_SCALE: return launch_ll_staged_t<EP_FP8_E4M3_F32_SCALE>(p, stream);
+    case EP_FP8_E4M3_UE8M0: return launch_ll_staged_t<EP_FP8_E4M3_UE8M0>(p, stream);
+  }
+  return EP_ERR_INVALID_ARG;
+}
+
+// ------------------------------------------------------------------ scale columns
+
+struct ScaleColParams {
+  const uint8_t* scale_rows;   // [T][row_bytes] per-token scales
+  int row_bytes, nb;
+  int64_t T;
+  int64_t seg_rows;
+  int64_t n_rows;              // rows of the receive buffer (segments * seg_rows)
+  const int32_t* src_idx;      // token of every receive row, -1 = none (normal mode)
+  const int32_t* recv_count;   // low-latency mode: rows per expert segment (src_idx
+                               // is only defined below it)
+  void* out;                   // column-major scales [segment][block][row]
+};
+
+constexpr int kScaleMaxGroups = 8;   // 16-byte groups of a staged scale row held at once
+
+// Flat over receive rows, one lane per row: a row holding a token gathers
+// that token's staged scales (16-byte loads, all issued before any store) and
+// writes them down its column entries -- consecutive lanes write consecutive
+// rows, so every store instruction is coalesced, and skewed routing (one
+// expert with most rows) spreads over all CTAs.
+template <bool kLL, int kEs>
+__global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColParams p) {
+  pdl_wait();   // the scatter's staged scales and row sources
+  constexpr int kPer16 = 16 / kEs;   // scale values per 16-byte group
+  const int ngrp = p.row_bytes / 16;
+  // low-latency: grid (expert, row block) over the rows below recv_count;
+  // normal: flat over all rows (recv_src_idx is -1 where no token sits)
+  int64_t f = kLL ? (int64_t)blockIdx.x * p.seg_rows + (int64_t)blockIdx.y * kScaleColThreads + threadIdx.x
+                  : (int64_t)blockIdx.x * kScaleColThreads + threadIdx.x;
+  const int64_t stride = kLL ? p.n_rows : (int64_t)gridDim.x * kScaleColThreads;
+  if (kLL && (int64_t)blockIdx.y * kScaleColThreads >= (int64_t)__ldg(&p.recv_count[blockIdx.x])) return;
+  for (; f < p.n_rows; f += stride) {
+    const int64_t seg = kLL ? (int64_t)blockIdx.x : f / p.seg_rows;
+    const int64_t row = f - seg * p.seg_rows;
+    bool valid = true;
+    if (kLL) valid = row < p.seg_rows && row < (int64_t)__ldg(&p.recv_count[seg]);
+    const int64_t src = valid ? (int64_t)__ldg(&p.src_idx[f]) : -1;
+    valid = src >= 0 && src < p.T;
+    const uint8_t* srow = p.scale_rows + src * p.row_bytes;
+    for (int g0 = 0; g0 < ngrp; g0 += kScaleMaxGroups) {
+      uint4 v[kScaleMaxGroups];
+#pragma unroll
+      for (int u = 0; u < kScaleMaxGroups; ++u)
+        v[u] = (valid && g0 + u < ngrp) ? __ldg(reinterpret_cast<const uint4*>(srow) + g0 + u)
+                                        : make_uint4(0, 0, 0, 0);
+      if (!valid) continue;
+#pragma unroll
+      for (int u = 0; u < kScaleMaxGroups; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int t = 0; t < kPer16; ++t) {
+          const int b = (g0 + u) * kPer16 + t;
+          if (b < p.nb) {
+            const int64_t o = (seg * p.nb + b) * p.seg_rows + row;
+            if (kEs == 4) static_cast<uint32_t*>(p.out)[o] = w[t];
+            else static_cast<uint8_t*>(p.out)[o] = (uint8_t)(w[t >> 2] >> (8 * (t & 3)));
+          }
+        }
+      }
+    }
+  }
+}
+
+template <bool kLL, int kEs>
+static int launch_scale_columns_t(const ScaleColParams& p, cudaStream_t stream) {
+  dim3 grid;
+  if (kLL) {
+    grid = dim3((unsigned)(p.n_rows / p.seg_rows),
+                (unsigned)((p.seg_rows + kScaleColThreads - 1) / kScaleColThreads));
+  } else {
+    const int64_t want = (p.n_rows + kScaleColThreads - 1) / kScaleColThreads;
+    grid = dim3((unsigned)std::max<int64_t>(
+        1, std::min<int64_t>(want, (int64_t)ep_host::num_sms() * 8)));
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kScaleColThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_scale_columns<kLL, kEs>, p) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
+  ep_host::count_launch();
+  return ep_host::check_launch();
+}
+
+static int launch_scale_columns(const ScaleColParams& p, bool ll, int fp8_mode, cudaStream_t s) {
+  const bool f32 = fp8_mode == EP_FP8_E4M3_F32_SCALE;
+  if (ll) return f32 ? launch_scale_columns_t<true, 4>(p, s) : launch_scale_columns_t<true, 1>(p, s);
+  return f32 ? launch_scale_columns_t<false, 4>(p, s) : launch_scale_columns_t<false, 1>(p, s);
+}
+
+// ------------------------------------------------------------------ launch
+
+// Piece size, per-warp shared memory and warps per CTA: the largest piece
+// (a multiple of the 16-byte / 128-channel granule) whose stages fit the
+// per-warp share of `budget` for `target_warps` warps.
+static void plan_pipeline(ScatterParams& p, int fp8_mode, int target_warps, size_t budget) {
+  const bool fp8 = fp8_mode != EP_FP8_NONE;
+  const int gran = fp8 ? kFp8Block : 8;
+  const int ns = fp8 ? kFp8InStages : kBf16Stages;
+  const int no = fp8 ? kFp8OutStages : 1;
+  auto warp_bytes = [&](int hp, uint32_t* in_b, uint32_t* out_b) {
+    *in_b = round128((uint32_t)hp * 2u);
+    *out_b = fp8 ? round128((uint32_t)hp) : 0u;
+    return (size_t)ns * *in_b + (size_t)no * *out_b + 128;
+  };
+  const size_t per_warp = budget / (size_t)target_warps;
+  uint32_t in_b, out_b;
+  int P = 1;
+  int hp = p.H;
+  while (hp > gran && warp_bytes(hp, &in_b, &out_b) > per_warp) {
+    ++P;
+    hp = ((p.H + P - 1) / P + gran - 1) / gran * gran;
+  }
+  P = (p.H + hp - 1) / hp;
+  const size_t wb = warp_bytes(hp, &in_b, &out_b);
+  p.Hp = hp;
+  p.P = P;
+  p.in_bytes = in_b;
+  p.out_bytes = out_b;
+  p.warp_smem = (uint32_t)wb;
+  p.warps_per_cta = (int)std::max<size_t>(1, std::min<size_t>((size_t)kScatterMaxWarps, budget / wb));
+}
+
+template <int kMode, bool kLL>
+static int launch_scatter_t(ScatterParams p, cudaStream_t stream, bool pdl) {
+  plan_pipeline(p, kMode, kMode == EP_FP8_NONE ? kBf16Warps : kFp8Warps, kScatterSmemBudget);
+  p.n_units = p.T * p.P;
+  if (p.n_units > INT32_MAX) return EP_ERR_INVALID_ARG;
+  const size_t smem = (size_t)p.warps_per_cta * p.warp_smem;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_scatter<kMode, kLL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kScatterSmemBudget + 1024) != cudaSuccess) {
+      cudaGetLastError();
+      return EP_ERR_CUDA;
+    }
+    attr_set = true;
+  }
+  const int64_t work = std::max<int64_t>(p.n_units, p.n_pad_items);
+  const int64_t want = (work + p.warps_per_cta - 1) / p.warps_per_cta;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::num_sms()));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kScatterThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(p.warps_per_cta * kWarp);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -257,21 +827,39 @@ static int check_common(int R, int T_r, int H, int E, int k, int fp8_mode) {
   return EP_OK;
 }
 
+// Staged per-token scales live after the layout kernel's region of the
+// workspace (the two never alias).
+static uint8_t* scale_staging(void* ws, int R, int T_r, int k, int E) {
+  return static_cast<uint8_t*>(ws) + layout_geometry(R, T_r, k, E).bytes;
+}
+
 }  // namespace ep
+
+extern "C" size_t ep_workspace_size(int R, int T_r, int k, int E, int H) {
+  if (R <= 0 || k <= 0 || k > ep::kMaxK || E <= 0 || T_r < 0 || H <= 0) return 0;
+  const size_t staging = (size_t)R * T_r * ep::scale_row_bytes(H, 4);
+  return ep::layout_geometry(R, T_r, k, E).bytes + (staging + 255) / 256 * 256;
+}
 
 extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t* slot_rank,
                            const int32_t* expert_prefix, const int64_t* psum, int R, int T_r,
                            int H, int E, int k, int fp8_mode, int64_t cap_rows, void* recv_x,
                            void* recv_scales, int32_t* recv_src_idx, int32_t* combine_idx,
-                           int32_t* status, void* stream) {
+                           void* workspace, size_t workspace_bytes, int32_t* status,
+                           void* stream) {
   int rc = ep::check_common(R, T_r, H, E, k, fp8_mode);
   if (rc != EP_OK) return rc;
   if (cap_rows < 0 || (int64_t)R * cap_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
+  const bool fp8 = fp8_mode != EP_FP8_NONE;
   if (!expert_prefix || !psum || !recv_src_idx ||
       (T_r > 0 && (!x || !topk_idx || !slot_rank || !combine_idx)) ||
-      (cap_rows > 0 && !recv_x) || (fp8_mode != EP_FP8_NONE && cap_rows > 0 && !recv_scales))
+      (cap_rows > 0 && !recv_x) || (fp8 && cap_rows > 0 && !recv_scales))
     return EP_ERR_INVALID_ARG;
-  if (!ep_host::aligned16(x) || !ep_host::aligned16(recv_x)) return EP_ERR_INVALID_ARG;
+  if (fp8 && (!workspace || workspace_bytes < ep_workspace_size(R, T_r, k, E, H)))
+    return EP_ERR_INVALID_ARG;
+  if (!ep_host::aligned16(x) || !ep_host::aligned16(recv_x) || !ep_host::aligned16(workspace))
+    return EP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   ep::ScatterParams p{};
   p.x = static_cast<const uint8_t*>(x);
   p.R = R;
@@ -281,7 +869,6 @@ extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t
   p.E_l = E / R;
   p.k = k;
   p.T = (int64_t)R * T_r;
-  p.nseg = (H + ep::kScatterSegC - 1) / ep::kScatterSegC;
   p.topk_idx = topk_idx;
   p.slot_rank = slot_rank;
   p.expert_prefix = expert_prefix;
@@ -289,14 +876,28 @@ extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t
   p.seg_rows = cap_rows;
   p.n_rows = (int64_t)R * cap_rows;
   p.recv_x = static_cast<uint8_t*>(recv_x);
-  p.recv_scales = recv_scales;
   p.recv_src_idx = recv_src_idx;
   p.combine_idx = combine_idx;
+  const int es = fp8_mode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
+  if (fp8) {
+    p.scale_rows = ep::scale_staging(workspace, R, T_r, k, E);
+    p.scale_row_bytes = ep::scale_row_bytes(H, es);
+  }
   p.status = status;
-  p.n_items = p.T * p.nseg;
   p.tail_chunks = (int)((cap_rows + ep::kPadChunkRows - 1) / ep::kPadChunkRows);
   p.n_pad_items = (int64_t)R * p.E_l + (int64_t)R * p.tail_chunks;
-  return ep::launch_scatter(p, fp8_mode, false, static_cast<cudaStream_t>(stream));
+  rc = ep::launch_scatter(p, fp8_mode, false, s);
+  if (rc != EP_OK || !fp8 || cap_rows == 0) return rc;
+  ep::ScaleColParams sp{};
+  sp.scale_rows = p.scale_rows;
+  sp.row_bytes = p.scale_row_bytes;
+  sp.nb = H / ep::kFp8Block;
+  sp.T = p.T;
+  sp.seg_rows = cap_rows;
+  sp.n_rows = (int64_t)R * cap_rows;
+  sp.src_idx = recv_src_idx;
+  sp.out = recv_scales;
+  return ep::launch_scale_columns(sp, false, fp8_mode, s);
 }
 
 extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int T_r, int H, int E,
@@ -310,14 +911,18 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
   if (max_tokens_per_rank <= 0 || T_r > max_tokens_per_rank) return EP_ERR_INVALID_ARG;
   const int64_t seg_rows = (int64_t)R * max_tokens_per_rank;
   if ((int64_t)E * seg_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
+  const bool fp8 = fp8_mode != EP_FP8_NONE;
   if (!packed_recv_x || !packed_recv_src_info || !layout_range || !recv_count || !workspace ||
-      (T_r > 0 && (!x || !topk_idx || !combine_idx)) ||
-      (fp8_mode != EP_FP8_NONE && !packed_recv_scales))
+      (T_r > 0 && (!x || !topk_idx || !combine_idx)) || (fp8 && !packed_recv_scales))
     return EP_ERR_INVALID_ARG;
-  if (!ep_host::aligned16(x) || !ep_host::aligned16(packed_recv_x)) return EP_ERR_INVALID_ARG;
-  if (workspace_bytes < ep_workspace_size(R, T_r, k, E)) return EP_ERR_INVALID_ARG;
+  if (!ep_host::aligned16(x) || !ep_host::aligned16(packed_recv_x) ||
+      !ep_host::aligned16(workspace))
+    return EP_ERR_INVALID_ARG;
+  if (workspace_bytes < ep_workspace_size(R, T_r, k, E, H)) return EP_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+  // multi-CTA look-back layout; the scatter follows as its programmatic
+  // dependent launch, the scale columns as the scatter's.
   ep::LayoutParams lp{};
   lp.topk_idx = topk_idx;
   lp.R = R;
@@ -343,15 +948,31 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
   p.E_l = E / R;
   p.k = k;
   p.T = (int64_t)R * T_r;
-  p.nseg = (H + ep::kScatterSegC - 1) / ep::kScatterSegC;
   p.seg_rows = seg_rows;
   p.n_rows = (int64_t)E * seg_rows;
   p.recv_x = static_cast<uint8_t*>(packed_recv_x);
-  p.recv_scales = packed_recv_scales;
   p.combine_idx = combine_idx;
+  const int es = fp8_mode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
+  if (fp8) {
+    p.scale_rows = ep::scale_staging(workspace, R, T_r, k, E);
+    p.scale_row_bytes = ep::scale_row_bytes(H, es);
+  }
   p.status = status;
-  p.n_items = p.T * p.nseg;
   p.n_pad_items = 0;
-  if (p.n_items == 0) return EP_OK;
-  return ep::launch_scatter(p, fp8_mode, true, s);
+  if (p.T == 0) return EP_OK;
+  ep::ScatterParams ps = p;
+  rc = ep::plan_staged(ps) ? ep::launch_ll_staged(ps, fp8_mode, s)
+                                     : ep::launch_scatter(p, fp8_mode, true, s);
+  if (rc != EP_OK || !fp8) return rc;
+  ep::ScaleColParams sp{};
+  sp.scale_rows = p.scale_rows;
+  sp.row_bytes = p.scale_row_bytes;
+  sp.nb = H / ep::kFp8Block;
+  sp.T = p.T;
+  sp.seg_rows = seg_rows;
+  sp.n_rows = (int64_t)E * seg_rows;
+  sp.src_idx = packed_recv_src_info;
+  sp.recv_count = recv_count;
+  sp.out = packed_recv_scales;
+  return ep::launch_scale_columns(sp, true, fp8_mode, s);
 }

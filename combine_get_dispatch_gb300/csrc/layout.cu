@@ -9,8 +9,9 @@
 // T*k ids with E buckets, done here as one kernel:
 //   1. a CTA takes a chunk of tokens (claimed through an atomic ticket, so
 //      chunks start in order and every wait below is on an earlier,
-//      already-running CTA), ranks its ids per warp with __match_any_sync
-//      and reduces the per-warp counts in shared memory;
+//      already-running CTA), ranks its ids per warp with equal-key lane
+//      masks built from ballots (peers_mask) and reduces the per-warp counts
+//      in shared memory;
 //   2. it publishes the chunk aggregate and looks back over the previous
 //      chunks' published (aggregate | inclusive) words, 8 at a time, to get
 //      its exclusive prefix per expert (decoupled look-back);
@@ -32,11 +33,11 @@
 
 namespace ep {
 
-constexpr int kLayoutThreads = 256;
+constexpr int kLayoutThreads = 512;
 constexpr int kLayoutWarps = kLayoutThreads / kWarp;
 constexpr int kMaxChunkIds = 2048;
-constexpr int kIdsPerLane = kMaxChunkIds / kLayoutThreads;   // 8
-constexpr int kLookbackWindow = 8;
+constexpr int kIdsPerLane = kMaxChunkIds / kLayoutThreads;   // 4
+constexpr int kLookbackWindow = 16;
 
 enum : uint32_t { kFlagAggregate = 1, kFlagInclusive = 2 };
 
@@ -72,18 +73,18 @@ __device__ __forceinline__ uint64_t wait_flag(const uint64_t* addr, uint64_t f, 
 }
 
 template <bool kLL>
-__global__ void __launch_bounds__(kLayoutThreads) k_layout(LayoutParams p) {
+__global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
   extern __shared__ int32_t smem[];
   int32_t* s_ids = smem;                                  // [kMaxChunkIds]
   int32_t* s_cnt = s_ids + kMaxChunkIds;                  // [warps][E]
   int32_t* s_agg = s_cnt + kLayoutWarps * p.E;            // [V]
   int32_t* s_excl = s_agg + p.V;                          // [V]
   __shared__ uint32_t s_ticket, s_epoch;
-  __shared__ int s_last;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
+  const int nbits = key_bits(p.E);
 
   if (kLL) pdl_launch_dependents();   // the scatter kernel may start loading x
   if (tid == 0) {
@@ -110,13 +111,28 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(LayoutParams p) {
   const int n = nt * p.k;
   const int64_t id_base = ((int64_t)i * p.T_r + t0) * p.k;
 
-  // ---- 1. load the chunk's ids (validated) into shared memory
-  for (int q = tid; q < n; q += kLayoutThreads) {
-    int64_t e = p.topk_idx[id_base + q];
-    int v = -1;
-    if (e >= 0 && e < p.E) v = (int)e;
-    else if (e != -1) set_status(p.status, EP_ERR_INVALID_ARG);
-    s_ids[q] = v;
+  // ---- 1. load the chunk's ids (validated) into shared memory; all loads
+  //      of a thread are issued before the first is used
+  {
+    int64_t ev[kIdsPerLane];
+#pragma unroll
+    for (int u = 0; u < kIdsPerLane; ++u) {
+      const int q = tid + u * kLayoutThreads;
+      ev[u] = q < n ? __ldg(&p.topk_idx[id_base + q]) : -1;
+    }
+    bool bad = false;
+#pragma unroll
+    for (int u = 0; u < kIdsPerLane; ++u) {
+      const int q = tid + u * kLayoutThreads;
+      if (q < n) {
+        const int64_t e = ev[u];
+        int v = -1;
+        if (e >= 0 && e < p.E) v = (int)e;
+        else bad |= (e != -1);
+        s_ids[q] = v;
+      }
+    }
+    if (bad) set_status(p.status, EP_ERR_INVALID_ARG);
   }
   __syncthreads();
 
@@ -130,7 +146,7 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(LayoutParams p) {
     if (u * kWarp < per_warp) {
       const int q = wbase + u * kWarp + lane;
       const int e = (q < n) ? s_ids[q] : -1;
-      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      const uint32_t peers = peers_mask(e, nbits);
       int r = 0;
       if (e >= 0) r = s_cnt[warp * p.E + e] + __popc(peers & lanemask_lt());
       __syncwarp();
@@ -237,44 +253,45 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(LayoutParams p) {
       }
     }
   }
-  if (c == p.chunks_per_rank - 1) {     // last chunk of rank i: rank totals
-    if (kLL) {
-      for (int e = tid; e < p.E; e += kLayoutThreads)
-        p.rank_end[(size_t)i * p.E + e] = s_excl[e] + s_agg[e];
-    } else {
-      for (int e = tid; e < p.E; e += kLayoutThreads)
-        p.num_tokens_per_expert[(size_t)i * p.E + e] = s_excl[e] + s_agg[e];
-      for (int r = tid; r < p.R; r += kLayoutThreads)
-        p.num_tokens_per_rank[(size_t)i * p.R + r] = s_excl[p.E + r] + s_agg[p.E + r];
+  if (kLL && p.chunks_per_rank == 1) {
+    // the chunk is the whole rank: both ends of its range are known here
+    for (int e = tid; e < p.E; e += kLayoutThreads) {
+      const uint32_t lo = (uint32_t)s_excl[e];
+      const uint32_t hi = lo + (uint32_t)s_agg[e];
+      p.layout_range[(size_t)e * p.R + i] = ((int64_t)lo << 32) | (int64_t)(hi - lo);
+      if (i == p.R - 1) p.recv_count[e] = (int32_t)hi;
     }
-  }
-  if (kLL && c == 0) {
-    for (int e = tid; e < p.E; e += kLayoutThreads) p.rank_start[(size_t)i * p.E + e] = s_excl[e];
-  }
-
-  // ---- the last CTA to finish resets the ticket state (and, in low-latency
-  //      mode, writes recv_count and layout_range from the rank boundaries)
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t d = atomicAdd(&p.ctl[1], 1u);
-    s_last = (d == (uint32_t)p.num_chunks - 1);
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    if (kLL) {
+  } else if (kLL) {
+    // rank boundaries for layout_range: the first chunk of rank i publishes
+    // expert_prefix[i][e] (its exclusive prefix) as a tagged word; the last
+    // chunk of rank i pairs it with its inclusive prefix.
+    if (c == 0) {
+      for (int e = tid; e < p.E; e += kLayoutThreads)
+        st_relaxed_u64(&p.rank_start[(size_t)i * p.E + e],
+                       pack_flag(epoch, kFlagInclusive, (uint32_t)s_excl[e]));
+    }
+    if (c == p.chunks_per_rank - 1) {
       for (int e = tid; e < p.E; e += kLayoutThreads) {
-        for (int r = 0; r < p.R; ++r) {
-          const int32_t lo = ld_cg_i32(&p.rank_start[(size_t)r * p.E + e]);
-          const int32_t hi = ld_cg_i32(&p.rank_end[(size_t)r * p.E + e]);
-          p.layout_range[(size_t)e * p.R + r] = ((int64_t)lo << 32) | (int64_t)(uint32_t)(hi - lo);
-        }
-        p.recv_count[e] = ld_cg_i32(&p.rank_end[(size_t)(p.R - 1) * p.E + e]);
+        const uint64_t* a = &p.rank_start[(size_t)i * p.E + e];
+        const uint32_t lo =
+            (uint32_t)wait_flag(a, ld_relaxed_u64(a), epoch, &p.ctl[3], p.status);
+        const uint32_t hi = (uint32_t)(s_excl[e] + s_agg[e]);
+        p.layout_range[(size_t)e * p.R + i] = ((int64_t)lo << 32) | (int64_t)(hi - lo);
+        if (i == p.R - 1) p.recv_count[e] = (int32_t)hi;
       }
     }
-    if (tid == 0) {
+  } else if (c == p.chunks_per_rank - 1) {     // last chunk of rank i: rank totals
+    for (int e = tid; e < p.E; e += kLayoutThreads)
+      p.num_tokens_per_expert[(size_t)i * p.E + e] = s_excl[e] + s_agg[e];
+    for (int r = tid; r < p.R; r += kLayoutThreads)
+      p.num_tokens_per_rank[(size_t)i * p.R + r] = s_excl[p.E + r] + s_agg[p.E + r];
+  }
+
+  // ---- the last CTA to finish resets the ticket state for the next launch
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t d = atomicAdd(&p.ctl[1], 1u);
+    if (d == (uint32_t)p.num_chunks - 1) {
       p.ctl[0] = 0;
       p.ctl[1] = 0;
       p.ctl[2] = s_epoch + 1;
@@ -293,8 +310,7 @@ LayoutGeometry layout_geometry(int R, int T_r, int k, int E) {
   g.V = E + R;
   g.flags_offset = 256;
   g.rank_start_offset = g.flags_offset + (size_t)g.num_chunks * g.V * sizeof(uint64_t);
-  g.rank_end_offset = g.rank_start_offset + (size_t)R * E * sizeof(int32_t);
-  g.bytes = (g.rank_end_offset + (size_t)R * E * sizeof(int32_t) + 255) / 256 * 256;
+  g.bytes = (g.rank_start_offset + (size_t)R * E * sizeof(uint64_t) + 255) / 256 * 256;
   return g;
 }
 
@@ -308,8 +324,7 @@ int launch_layout(const LayoutParams& p_in, bool ll, void* ws, cudaStream_t stre
   const LayoutGeometry g = layout_geometry(p.R, p.T_r, p.k, p.E);
   p.ctl = reinterpret_cast<uint32_t*>(base);
   p.flags = reinterpret_cast<uint64_t*>(base + g.flags_offset);
-  p.rank_start = reinterpret_cast<int32_t*>(base + g.rank_start_offset);
-  p.rank_end = reinterpret_cast<int32_t*>(base + g.rank_end_offset);
+  p.rank_start = reinterpret_cast<uint64_t*>(base + g.rank_start_offset);
   p.chunk_tokens = g.chunk_tokens;
   p.chunks_per_rank = g.chunks_per_rank;
   p.num_chunks = (int)g.num_chunks;
@@ -331,11 +346,6 @@ int launch_layout(const LayoutParams& p_in, bool ll, void* ws, cudaStream_t stre
 
 }  // namespace ep
 
-extern "C" size_t ep_workspace_size(int R, int T_r, int k, int E) {
-  if (R <= 0 || k <= 0 || k > ep::kMaxK || E <= 0 || T_r < 0) return 0;
-  return ep::layout_geometry(R, T_r, k, E).bytes;
-}
-
 extern "C" int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E,
                                       int32_t* num_tokens_per_rank,
                                       int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
@@ -347,7 +357,7 @@ extern "C" int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, i
   if (!num_tokens_per_rank || !num_tokens_per_expert || !workspace ||
       (T_r > 0 && (!topk_idx || !is_token_in_rank || !slot_rank)))
     return EP_ERR_INVALID_ARG;
-  if (workspace_bytes < ep_workspace_size(R, T_r, k, E)) return EP_ERR_INVALID_ARG;
+  if (workspace_bytes < ep::layout_geometry(R, T_r, k, E).bytes) return EP_ERR_INVALID_ARG;
   ep::LayoutParams p{};
   p.topk_idx = topk_idx;
   p.R = R;

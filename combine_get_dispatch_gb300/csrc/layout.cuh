@@ -25,8 +25,7 @@ struct LayoutParams {
   // workspace views
   uint32_t* ctl;        // [0] ticket, [1] finished CTAs, [2] launch epoch, [3] abort
   uint64_t* flags;      // [num_chunks][V] look-back words
-  int32_t* rank_start;  // [R][E] low-latency: prefix at the start of each rank
-  int32_t* rank_end;    // [R][E] low-latency: prefix at the end of each rank
+  uint64_t* rank_start;  // [R][E] low-latency: tagged prefix at the start of each rank
   int32_t* status;
 };
 
@@ -35,10 +34,14 @@ struct LayoutGeometry {
   int chunks_per_rank;
   int64_t num_chunks;
   int V;
-  size_t flags_offset, rank_start_offset, rank_end_offset, bytes;
+  size_t flags_offset, rank_start_offset, bytes;
 };
 
 LayoutGeometry layout_geometry(int R, int T_r, int k, int E);
+
+
+
+
 
 // Launch the layout kernel on workspace `ws` (normal: per-rank scan into
 // p's normal outputs; ll: global scan into p's low-latency outputs).

@@ -61,12 +61,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     if not os.path.exists(_build.LIB):
         raise RuntimeError(f"libep.so not found at {_build.LIB}; build it with __graft_entry__.build()")
     L = ctypes.CDLL(_build.LIB)
-    L.ep_workspace_size.argtypes = [_I, _I, _I, _I]
+    L.ep_workspace_size.argtypes = [_I, _I, _I, _I, _I]
     L.ep_workspace_size.restype = _SZ
     L.ep_get_dispatch_layout.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]
     L.ep_notify_dispatch.argtypes = [_P, _P, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _I, _P, _P]
     L.ep_dispatch.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I64, _P, _P, _P, _P,
-                              _P, _P]
+                              _P, _SZ, _P, _P]
     L.ep_combine.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I64, _P, _P, _P]
     L.ep_ll_dispatch.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                  _SZ, _P, _P]
@@ -125,8 +125,8 @@ def _scale_dtype(fp8_mode: int):
 
 # ------------------------------------------------------------------ entry points
 
-def ep_workspace_size(R: int, T_r: int, k: int, E: int) -> int:
-    return int(load().ep_workspace_size(R, T_r, k, E))
+def ep_workspace_size(R: int, T_r: int, k: int, E: int, H: int) -> int:
+    return int(load().ep_workspace_size(R, T_r, k, E, H))
 
 
 def ep_get_dispatch_layout(topk_idx, num_experts, num_tokens_per_rank, num_tokens_per_expert,
@@ -173,7 +173,8 @@ def ep_notify_dispatch(num_tokens_per_rank, num_tokens_per_expert, expert_alignm
 
 
 def ep_dispatch(x, topk_idx, slot_rank, expert_prefix, psum, num_experts, fp8_mode, cap_rows,
-                recv_x, recv_scales, recv_src_idx, combine_idx, status=None, stream=None):
+                recv_x, recv_scales, recv_src_idx, combine_idx, workspace=None, status=None,
+                stream=None):
     R, T_r, H = x.shape
     k = topk_idx.shape[2]
     E = num_experts
@@ -189,11 +190,14 @@ def ep_dispatch(x, topk_idx, slot_rank, expert_prefix, psum, num_experts, fp8_mo
         _need(recv_scales, _scale_dtype(fp8_mode), (R, H // 128, cap_rows), "recv_scales")
     _need(recv_src_idx, torch.int32, (R, cap_rows), "recv_src_idx")
     _need(combine_idx, torch.int32, (R, T_r, k), "combine_idx")
+    _need(workspace, torch.uint8, name="workspace", optional=fp8_mode == EP_FP8_NONE)
     _need(status, torch.int32, (1,), "status", optional=True)
     rc = load().ep_dispatch(_ptr(x), _ptr(topk_idx), _ptr(slot_rank), _ptr(expert_prefix),
                             _ptr(psum), R, T_r, H, E, k, fp8_mode, cap_rows, _ptr(recv_x),
                             _ptr(recv_scales) if fp8_mode != EP_FP8_NONE else None,
-                            _ptr(recv_src_idx), _ptr(combine_idx), _ptr(status), _stream(stream))
+                            _ptr(recv_src_idx), _ptr(combine_idx), _ptr(workspace),
+                            0 if workspace is None else workspace.numel(), _ptr(status),
+                            _stream(stream))
     _check(rc, "ep_dispatch")
 
 
@@ -334,8 +338,8 @@ def alloc_ll(R: int, T_r: int, H: int, E: int, k: int, max_tokens_per_rank: int,
     )
 
 
-def alloc_workspace(R: int, T_r: int, k: int, E: int, device="cuda", stream=None):
-    """Workspace for layout / low-latency dispatch, cleaned and ready."""
-    ws = torch.empty((ep_workspace_size(R, T_r, k, E),), dtype=torch.uint8, device=device)
+def alloc_workspace(R: int, T_r: int, k: int, E: int, H: int, device="cuda", stream=None):
+    """Workspace for layout and dispatch (ep_workspace_size), cleaned and ready."""
+    ws = torch.empty((ep_workspace_size(R, T_r, k, E, H),), dtype=torch.uint8, device=device)
     ep_clean_ll_buffer(None, R, E, ws, stream=stream)
     return ws

@@ -64,13 +64,15 @@ extern "C" {
 #define EP_FP8_E4M3_F32_SCALE 1
 #define EP_FP8_E4M3_UE8M0 2
 
-/* Bytes of device workspace that ep_get_dispatch_layout and ep_ll_dispatch
- * need for problems up to (R, T_r, k, E).  The workspace holds the
- * cross-block prefix (decoupled look-back) state; it must be zeroed once
- * with ep_clean_ll_buffer before its first use, after which every call
- * leaves it ready for the next.  Calls that share one workspace must be
- * ordered on one stream (overlapping calls race). */
-size_t ep_workspace_size(int R, int T_r, int k, int E);
+/* Bytes of device workspace that ep_get_dispatch_layout, ep_dispatch and
+ * ep_ll_dispatch need for problems up to (R, T_r, k, E, H); 0 for invalid
+ * sizes.  The workspace holds the cross-block prefix (decoupled look-back)
+ * state of the layout kernels and the per-token FP8 scales staged between
+ * the scatter and the column-major scale pass.  It must be zeroed once with
+ * ep_clean_ll_buffer before its first use, after which every call leaves it
+ * ready for the next.  Calls that share one workspace must be ordered on
+ * one stream (overlapping calls race).  16-byte aligned. */
+size_t ep_workspace_size(int R, int T_r, int k, int E, int H);
 
 /* get_dispatch_layout (§2.1; handle fields §2.3).  For every source rank i:
  *   num_tokens_per_rank   [R, R] int32: [i][r] = tokens of rank i that go to
@@ -118,12 +120,16 @@ int ep_notify_dispatch(const int32_t* num_tokens_per_rank, const int32_t* num_to
  *   recv_src_idx [R, cap_rows] int32: i*T_r + t for every filled row, -1 on
  *                alignment padding and past the last row
  *   combine_idx  [R, T_r, k] int32: r*cap_rows + row, -1 for an unused slot
+ *   workspace    ep_workspace_size bytes (required when fp8_mode > 0, may be
+ *                NULL for bf16)
  * A row at or past cap_rows is not written (EP_ERR_CAPACITY, slot -1).
- * Rows of recv_x / recv_scales that no slot fills are left untouched. */
+ * Rows of recv_x that no slot fills are left untouched; scale entries of
+ * rows that hold no token are unspecified. */
 int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t* slot_rank,
                 const int32_t* expert_prefix, const int64_t* psum, int R, int T_r, int H,
                 int E, int k, int fp8_mode, int64_t cap_rows, void* recv_x, void* recv_scales,
-                int32_t* recv_src_idx, int32_t* combine_idx, int32_t* status, void* stream);
+                int32_t* recv_src_idx, int32_t* combine_idx, void* workspace,
+                size_t workspace_bytes, int32_t* status, void* stream);
 
 /* Normal-mode combine (§1.1, §2.3: dispatch walked backwards):
  *   out[i][t][:] = bf16_rn( fp32 fma chain over j = 0..k-1 of

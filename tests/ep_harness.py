@@ -49,7 +49,7 @@ def gpu_layout(idx_dev: torch.Tensor, E: int, ws=None, status=None):
     out = ep.alloc_layout(R, T_r, k, E)
     for v in out.values():
         poison_(v)
-    ws = ws if ws is not None else ep.alloc_workspace(R, T_r, k, E)
+    ws = ws if ws is not None else ep.alloc_workspace(R, T_r, k, E, 8)
     status = status if status is not None else status_word()
     ep.ep_get_dispatch_layout(idx_dev, E, out["num_tokens_per_rank"], out["num_tokens_per_expert"],
                               out["is_token_in_rank"], out["slot_rank"], ws, status)
@@ -72,16 +72,17 @@ def gpu_notify(lay: dict, E: int, A: int = 1, num_worst_tokens: int = -1, host_r
     return out
 
 
-def gpu_dispatch(x_dev, idx_dev, lay, nt, E, fp8_mode, cap_rows, status=None):
+def gpu_dispatch(x_dev, idx_dev, lay, nt, E, fp8_mode, cap_rows, status=None, ws=None):
     R, T_r, H = x_dev.shape
     k = idx_dev.shape[2]
     out = ep.alloc_dispatch(R, T_r, H, k, fp8_mode, cap_rows)
     for v in out.values():
         poison_(v)
     status = status if status is not None else status_word()
+    ws = ws if ws is not None else ep.alloc_workspace(R, T_r, k, E, H)
     ep.ep_dispatch(x_dev, idx_dev, lay["slot_rank"], nt["expert_prefix"], nt["psum"], E, fp8_mode,
                    cap_rows, out["recv_x"], out["recv_scales"], out["recv_src_idx"],
-                   out["combine_idx"], status)
+                   out["combine_idx"], ws, status)
     out["status"] = status
     return out
 
@@ -93,7 +94,7 @@ def gpu_ll_dispatch(x_dev, idx_dev, E, max_tokens, fp8_mode, ws=None, status=Non
     for key, v in out.items():
         if key != "recv_count":
             poison_(v)
-    ws = ws if ws is not None else ep.alloc_workspace(R, T_r, k, E)
+    ws = ws if ws is not None else ep.alloc_workspace(R, T_r, k, E, H)
     status = status if status is not None else status_word()
     ep.ep_ll_dispatch(x_dev, idx_dev, E, max_tokens, fp8_mode, out["packed_recv_x"],
                       out["packed_recv_scales"], out["packed_recv_src_info"], out["layout_range"],

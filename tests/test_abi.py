@@ -48,11 +48,14 @@ def test_error_strings_and_launch_counter():
 
 
 def test_workspace_size():
-    a = ep.ep_workspace_size(16, 128, 8, 256)
-    b = ep.ep_workspace_size(16, 4096, 8, 256)
+    a = ep.ep_workspace_size(16, 128, 8, 256, 7168)
+    b = ep.ep_workspace_size(16, 4096, 8, 256, 7168)
     assert a > 0 and b > a and a % 256 == 0
-    assert ep.ep_workspace_size(0, 1, 1, 1) == 0
-    assert ep.ep_workspace_size(2, 1, 17, 4) == 0
+    # the FP8 scale staging grows with the hidden size
+    assert ep.ep_workspace_size(16, 128, 8, 256, 4096) < a
+    assert ep.ep_workspace_size(0, 1, 1, 1, 128) == 0
+    assert ep.ep_workspace_size(2, 1, 17, 4, 128) == 0
+    assert ep.ep_workspace_size(2, 1, 1, 4, 0) == 0
 
 
 def test_host_wait_counters_times_out_and_succeeds():
@@ -92,10 +95,10 @@ def test_argument_validation_returns_invalid_arg_without_launch():
     assert L.ep_notify_dispatch(None, None, 2, 8, 0, -1, None, None, None, None, None, 0, None,
                                 None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_dispatch(None, None, None, None, None, 2, 4, 7168, 8, 8, 1, 16, None, None, None,
-                         None, None, None) == ep.EP_ERR_INVALID_ARG
+                         None, None, 0, None, None) == ep.EP_ERR_INVALID_ARG
     # FP8 needs H % 128 == 0
     assert L.ep_dispatch(None, None, None, None, None, 2, 0, 200, 8, 8, 2, 0, None, None, None,
-                         None, None, None) == ep.EP_ERR_INVALID_ARG
+                         None, None, 0, None, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_ll_dispatch(None, None, 2, 8, 256, 8, 2, 4, 0, None, None, None, None, None, None,
                             None, 0, None, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_combine(None, None, None, 2, 4, 256, 0, 16, None, None,

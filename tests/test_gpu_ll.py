@@ -66,7 +66,11 @@ def test_ll_decode_full_size():
     (4, 700, 700, 4, 32, 256, 1),      # several chunks per rank (ragged)
     (8, 1, 1, 1, 8, 128, 0),           # one token per rank, one expert per rank
     (2, 0, 4, 2, 4, 128, 2),           # no tokens at all
-    (32, 256, 256, 6, 128, 4096, 1),   # the skewed workload's shape, low-latency
+    (32, 256, 256, 6, 128, 4096, 1),   # the skewed workload's shape
+    (16, 512, 512, 8, 256, 512, 2),    # larger chunks
+    (200, 3, 4, 2, 400, 256, 2),       # more ranks than chunks (one chunk per rank)
+    (16, 2048, 2048, 8, 256, 128, 2),  # chunks too large: layout kernel with look-back
+    (2, 10000, 10000, 8, 16, 128, 0),  # look-back path, ragged chunks
 ])
 def test_ll_shapes(R, T_r, max_tokens, k, E, H, fp8_mode):
     w = synth.Workload("t", R=R, T_r=T_r, H=H, E=E, k=k, routing="uniform", mode="ll",
@@ -106,9 +110,11 @@ def test_ll_bounded_wait_on_a_chunk_that_never_publishes():
     never published.  The other CTAs' waits must give up after their bound
     (EP_ERR_TIMEOUT / EP_ERR_STATE in the status word), the kernel must
     finish, and after ep_clean_ll_buffer the same workspace works again."""
-    w = synth.scaled(synth.WORKLOADS["decode"], T_r=128, H=128, fp8_mode=0)
+    # large enough for the layout kernel with look-back
+    w = synth.scaled(synth.WORKLOADS["decode"], T_r=2048, max_tokens_per_rank=2048, H=128,
+                     fp8_mode=0)
     x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
-    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E)
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
     ws[:4].view(torch.int32)[0] = 1            # ticket counter := 1
     d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, 0, ws=ws)
     torch.cuda.synchronize()
