@@ -79,6 +79,7 @@ extern "C" const char* ep_error_string(int code) {
     case EP_ERR_TIMEOUT: return "wait timed out";
     case EP_ERR_CUDA: return "CUDA error";
     case EP_ERR_STATE: return "workspace not initialised (call ep_clean_ll_buffer)";
+    case EP_ERR_TOO_LARGE: return "problem exceeds the no-allocation entry point's static scratch";
     default: return "unknown error";
   }
 }

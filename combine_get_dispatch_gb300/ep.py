@@ -25,6 +25,7 @@ EP_ERR_CAPACITY = 2
 EP_ERR_TIMEOUT = 3
 EP_ERR_CUDA = 4
 EP_ERR_STATE = 5
+EP_ERR_TOO_LARGE = 6
 
 EP_FP8_NONE = 0
 EP_FP8_E4M3_F32_SCALE = 1

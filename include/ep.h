@@ -51,6 +51,7 @@ extern "C" {
 #define EP_ERR_TIMEOUT 3
 #define EP_ERR_CUDA 4
 #define EP_ERR_STATE 5 /* workspace not cleaned (ep_clean_ll_buffer) */
+#define EP_ERR_TOO_LARGE 6 /* problem exceeds ep_get_dispatch_layout_no_alloc's scratch */
 
 /* FP8 modes of dispatch (§1.1 "FP8 dispatch, BF16 combine"; §1.2
  * round_scale / use_ue8m0).  Scales cover blocks of 128 channels and are
@@ -88,6 +89,27 @@ int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E
                            uint8_t* is_token_in_rank, int32_t* slot_rank,
                            void* workspace, size_t workspace_bytes, int32_t* status,
                            void* stream);
+
+/* ep_get_dispatch_layout for callers that cannot allocate device memory
+ * (graph capture in progress, allocator callbacks, runtimes that forbid the
+ * library any allocation).  No counterpart in the article: it is the same
+ * layout computation, same arguments and outputs as ep_get_dispatch_layout
+ * minus the workspace, which is replaced by a 4 MiB array inside libep
+ * (held on every GPU that loads the library, until the process exits).
+ *  - Returns EP_ERR_TOO_LARGE, launching nothing, when the problem's
+ *    look-back state exceeds the array (ep_workspace_size(R, T_r, k, E, 8)
+ *    minus the FP8 staging must fit in 4 MiB: e.g. R=8, T_r=16384, k=8,
+ *    E=256 fits).
+ *  - Allocates nothing: no cudaMalloc / cudaFree, no allocating library call.
+ *  - Every call shares the one array and clears the part it uses first
+ *    (stream-ordered); calls that overlap on the GPU race, so order them on
+ *    one stream.
+ *  - The first call on a device looks up the array's address with that
+ *    device current; make it before any stream capture begins. */
+int ep_get_dispatch_layout_no_alloc(const int64_t* topk_idx, int R, int T_r, int k, int E,
+                                    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                                    uint8_t* is_token_in_rank, int32_t* slot_rank,
+                                    int32_t* status, void* stream);
 
 /* notify_dispatch (§2.1, §2.3, §4.3): the count exchange and prefix sums.
  *   rank_prefix_matrix [R, R] int32: [i][j] = sum_{i' <= i} num_tokens_per_rank[i'][j]
