@@ -666,15 +666,17 @@ __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColPara
   const int ngrp = p.row_bytes / 16;
   // low-latency: grid (expert, row block) over the rows below recv_count;
   // normal: flat over all rows (recv_src_idx is -1 where no token sits)
-  int64_t f = kLL ? (int64_t)blockIdx.x * p.seg_rows + (int64_t)blockIdx.y * kScaleColThreads + threadIdx.x
+  // low-latency: one CTA per expert over its rows below recv_count;
+  // normal: flat over all rows (recv_src_idx is -1 where no token sits)
+  const int64_t lim = kLL ? min((int64_t)max(__ldg(&p.recv_count[blockIdx.x]), 0), p.seg_rows) : 0;
+  int64_t f = kLL ? (int64_t)blockIdx.x * p.seg_rows + threadIdx.x
                   : (int64_t)blockIdx.x * kScaleColThreads + threadIdx.x;
-  const int64_t stride = kLL ? p.n_rows : (int64_t)gridDim.x * kScaleColThreads;
-  if (kLL && (int64_t)blockIdx.y * kScaleColThreads >= (int64_t)__ldg(&p.recv_count[blockIdx.x])) return;
-  for (; f < p.n_rows; f += stride) {
+  const int64_t f_end = kLL ? (int64_t)blockIdx.x * p.seg_rows + lim : p.n_rows;
+  const int64_t stride = kLL ? kScaleColThreads : (int64_t)gridDim.x * kScaleColThreads;
+  for (; f < f_end; f += stride) {
     const int64_t seg = kLL ? (int64_t)blockIdx.x : f / p.seg_rows;
     const int64_t row = f - seg * p.seg_rows;
     bool valid = true;
-    if (kLL) valid = row < p.seg_rows && row < (int64_t)__ldg(&p.recv_count[seg]);
     const int64_t src = valid ? (int64_t)__ldg(&p.src_idx[f]) : -1;
     valid = src >= 0 && src < p.T;
     const uint8_t* srow = p.scale_rows + src * p.row_bytes;
@@ -706,8 +708,7 @@ template <bool kLL, int kEs>
 static int launch_scale_columns_t(const ScaleColParams& p, cudaStream_t stream) {
   dim3 grid;
   if (kLL) {
-    grid = dim3((unsigned)(p.n_rows / p.seg_rows),
-                (unsigned)((p.seg_rows + kScaleColThreads - 1) / kScaleColThreads));
+    grid = dim3((unsigned)(p.n_rows / p.seg_rows));
   } else {
     const int64_t want = (p.n_rows + kScaleColThreads - 1) / kScaleColThreads;
     grid = dim3((unsigned)std::max<int64_t>(
@@ -830,7 +831,7 @@ static int check_common(int R, int T_r, int H, int E, int k, int fp8_mode) {
 // Staged per-token scales live after the layout kernel's region of the
 // workspace (the two never alias).
 static uint8_t* scale_staging(void* ws, int R, int T_r, int k, int E) {
-  return static_cast<uint8_t*>(ws) + layout_geometry(R, T_r, k, E).bytes;
+  return static_cast<uint8_t*>(ws) + layout_region_bytes(R, T_r, k, E);
 }
 
 }  // namespace ep
@@ -838,7 +839,7 @@ static uint8_t* scale_staging(void* ws, int R, int T_r, int k, int E) {
 extern "C" size_t ep_workspace_size(int R, int T_r, int k, int E, int H) {
   if (R <= 0 || k <= 0 || k > ep::kMaxK || E <= 0 || T_r < 0 || H <= 0) return 0;
   const size_t staging = (size_t)R * T_r * ep::scale_row_bytes(H, 4);
-  return ep::layout_geometry(R, T_r, k, E).bytes + (staging + 255) / 256 * 256;
+  return ep::layout_region_bytes(R, T_r, k, E) + (staging + 255) / 256 * 256;
 }
 
 extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t* slot_rank,
@@ -962,7 +963,7 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
   if (p.T == 0) return EP_OK;
   ep::ScatterParams ps = p;
   rc = ep::plan_staged(ps) ? ep::launch_ll_staged(ps, fp8_mode, s)
-                                     : ep::launch_scatter(p, fp8_mode, true, s);
+                           : ep::launch_scatter(p, fp8_mode, true, s);
   if (rc != EP_OK || !fp8) return rc;
   ep::ScaleColParams sp{};
   sp.scale_rows = p.scale_rows;

@@ -33,11 +33,10 @@
 
 namespace ep {
 
-constexpr int kLayoutThreads = 512;
-constexpr int kLayoutWarps = kLayoutThreads / kWarp;
-constexpr int kMaxChunkIds = 2048;
-constexpr int kIdsPerLane = kMaxChunkIds / kLayoutThreads;   // 4
+constexpr int kIdsPerLane = 4;            // ids per thread per chunk
 constexpr int kLookbackWindow = 16;
+constexpr int kSmallLLThreads = 256;       // low-latency batches up to kSmallLLMaxIds
+constexpr int64_t kSmallLLMaxIds = 32768;
 
 enum : uint32_t { kFlagAggregate = 1, kFlagInclusive = 2 };
 
@@ -72,8 +71,10 @@ __device__ __forceinline__ uint64_t wait_flag(const uint64_t* addr, uint64_t f, 
   return pack_flag(epoch, kFlagAggregate, 0);
 }
 
-template <bool kLL>
+template <bool kLL, int kLayoutThreads>
 __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
+  constexpr int kLayoutWarps = kLayoutThreads / kWarp;
+  constexpr int kMaxChunkIds = kLayoutThreads * kIdsPerLane;
   extern __shared__ int32_t smem[];
   int32_t* s_ids = smem;                                  // [kMaxChunkIds]
   int32_t* s_cnt = s_ids + kMaxChunkIds;                  // [warps][E]
@@ -302,9 +303,9 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
 
 // ------------------------------------------------------------------ host side
 
-LayoutGeometry layout_geometry(int R, int T_r, int k, int E) {
+LayoutGeometry layout_geometry(int R, int T_r, int k, int E, int chunk_ids) {
   LayoutGeometry g;
-  g.chunk_tokens = kMaxChunkIds / k;
+  g.chunk_tokens = chunk_ids / k;
   g.chunks_per_rank = T_r > 0 ? (T_r + g.chunk_tokens - 1) / g.chunk_tokens : 1;
   g.num_chunks = (int64_t)R * g.chunks_per_rank;
   g.V = E + R;
@@ -314,34 +315,51 @@ LayoutGeometry layout_geometry(int R, int T_r, int k, int E) {
   return g;
 }
 
-static size_t layout_smem_bytes(int E, int V) {
-  return sizeof(int32_t) * ((size_t)kMaxChunkIds + (size_t)kLayoutWarps * E + 2 * (size_t)V);
+static bool small_ll(int R, int T_r, int k) {
+  return (int64_t)R * T_r * k <= kSmallLLMaxIds;
 }
 
-int launch_layout(const LayoutParams& p_in, bool ll, void* ws, cudaStream_t stream) {
-  LayoutParams p = p_in;
+size_t layout_region_bytes(int R, int T_r, int k, int E) {
+  size_t b = layout_geometry(R, T_r, k, E, kNormalChunkIds).bytes;
+  if (small_ll(R, T_r, k))
+    b = std::max(b, layout_geometry(R, T_r, k, E, kSmallLLThreads * kIdsPerLane).bytes);
+  return b;
+}
+
+template <bool kLL, int kThreads>
+static int launch_layout_t(LayoutParams p, void* ws, cudaStream_t stream) {
   char* base = static_cast<char*>(ws);
-  const LayoutGeometry g = layout_geometry(p.R, p.T_r, p.k, p.E);
+  const LayoutGeometry g = layout_geometry(p.R, p.T_r, p.k, p.E, kThreads * kIdsPerLane);
   p.ctl = reinterpret_cast<uint32_t*>(base);
   p.flags = reinterpret_cast<uint64_t*>(base + g.flags_offset);
   p.rank_start = reinterpret_cast<uint64_t*>(base + g.rank_start_offset);
   p.chunk_tokens = g.chunk_tokens;
   p.chunks_per_rank = g.chunks_per_rank;
   p.num_chunks = (int)g.num_chunks;
-  p.V = ll ? p.E : p.E + p.R;
-  const size_t smem = layout_smem_bytes(p.E, p.V);
-  auto kern = ll ? k_layout<true> : k_layout<false>;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[ll]) {
-    const int max_smem = (int)layout_smem_bytes(kMaxE, kMaxE + kMaxR);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-        cudaSuccess)
+  p.V = kLL ? p.E : p.E + p.R;
+  auto smem_bytes = [](int E, int V) {
+    return sizeof(int32_t) * ((size_t)kThreads * kIdsPerLane + (size_t)(kThreads / kWarp) * E + 2 * (size_t)V);
+  };
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_layout<kLL, kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes(kMaxE, kMaxE + kMaxR)) != cudaSuccess) {
+      cudaGetLastError();
       return EP_ERR_CUDA;
-    attr_set[ll] = true;
+    }
+    attr_set = true;
   }
-  kern<<<p.num_chunks, kLayoutThreads, smem, stream>>>(p);
+  k_layout<kLL, kThreads><<<p.num_chunks, kThreads, smem_bytes(p.E, p.V), stream>>>(p);
   ep_host::count_launch();
   return ep_host::check_launch();
+}
+
+int launch_layout(const LayoutParams& p, bool ll, void* ws, cudaStream_t stream) {
+  if (!ll) return launch_layout_t<false, kNormalChunkIds / kIdsPerLane>(p, ws, stream);
+  // decode-sized batches: smaller CTAs (they fit beside the scatter CTAs
+  // that follow as a programmatic dependent launch), 1024 ids per chunk
+  if (small_ll(p.R, p.T_r, p.k)) return launch_layout_t<true, kSmallLLThreads>(p, ws, stream);
+  return launch_layout_t<true, kNormalChunkIds / kIdsPerLane>(p, ws, stream);
 }
 
 }  // namespace ep
@@ -357,7 +375,8 @@ extern "C" int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, i
   if (!num_tokens_per_rank || !num_tokens_per_expert || !workspace ||
       (T_r > 0 && (!topk_idx || !is_token_in_rank || !slot_rank)))
     return EP_ERR_INVALID_ARG;
-  if (workspace_bytes < ep::layout_geometry(R, T_r, k, E).bytes) return EP_ERR_INVALID_ARG;
+  if (workspace_bytes < ep::layout_geometry(R, T_r, k, E, ep::kNormalChunkIds).bytes)
+    return EP_ERR_INVALID_ARG;
   ep::LayoutParams p{};
   p.topk_idx = topk_idx;
   p.R = R;

@@ -37,7 +37,12 @@ struct LayoutGeometry {
   size_t flags_offset, rank_start_offset, bytes;
 };
 
-LayoutGeometry layout_geometry(int R, int T_r, int k, int E);
+constexpr int kNormalChunkIds = 2048;   // ids per chunk (512 threads x 4)
+
+LayoutGeometry layout_geometry(int R, int T_r, int k, int E, int chunk_ids);
+
+// Workspace bytes the layout kernels use (the largest of their geometries).
+size_t layout_region_bytes(int R, int T_r, int k, int E);
 
 
 

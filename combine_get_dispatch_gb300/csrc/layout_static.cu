@@ -70,7 +70,7 @@ extern "C" int ep_get_dispatch_layout_no_alloc(const int64_t* topk_idx, int R, i
   if (R <= 0 || R > ep::kMaxR || E <= 0 || E > ep::kMaxE || E % R != 0 || k <= 0 ||
       k > ep::kMaxK || T_r < 0)
     return EP_ERR_INVALID_ARG;
-  const size_t bytes = ep::layout_geometry(R, T_r, k, E).bytes;
+  const size_t bytes = ep::layout_geometry(R, T_r, k, E, ep::kNormalChunkIds).bytes;
   if (bytes > kStaticScratchBytes) return EP_ERR_TOO_LARGE;
   if (!num_tokens_per_rank || !num_tokens_per_expert ||
       (T_r > 0 && (!topk_idx || !is_token_in_rank || !slot_rank)))
