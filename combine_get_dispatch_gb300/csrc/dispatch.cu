@@ -22,7 +22,9 @@
 //                      (packed row in (rank, token, slot) order, §1.2/§3.2)
 // and are fetched one / two units ahead of their use.  The low-latency
 // scatter is a programmatic dependent launch of the layout kernel: its first
-// bulk loads of x are issued before it waits for the layout.
+// bulk loads of x are issued before it waits for the layout.  Decode-size
+// low-latency batches skip all of this: k_ll_fused does layout, scatter and
+// scales in one launch (see its comment).
 //
 // Scales.  The receive layout keeps them column-major ([segment][block][row],
 // §1.2): one value per row and block at a stride of a whole column.  Stored
@@ -438,45 +440,291 @@ __global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterPar
   pad_fill(p, gw, W, lane);
 }
 
-// ------------------------------------------------------------------ staged low latency
+// ------------------------------------------------------------------ fused low latency
 
-constexpr int kStagedWarps = 16;
-constexpr int kStagedMaxPerWarp = 8;    // units per warp
-constexpr int kStagedPiece = 1024;      // channels per unit
+// Low-latency dispatch of a decode-size batch in ONE launch: routing layout,
+// scatter, FP8 quantisation and the column-major scales.  One CTA per SM;
+// the batch's (token, 1024-channel piece) units are split evenly over the
+// CTAs (a CTA's "own" tokens are those it holds a piece of), and every CTA
+//   0. loads the ids it needs and bulk-loads ALL its units' bf16 pieces at
+//      once (one shared-memory slot and one mbarrier per unit);
+//   1. CTA j < num_chunks histograms the j-th chunk of 1024 ids (in (rank,
+//      token, slot) order) and publishes it under a per-launch epoch; every
+//      CTA counts the ids between the start of the chunk holding its first
+//      own id and that id;
+//   2. (FP8) quantises each unit in place as it lands, staging the token's
+//      scales row-major in the workspace;
+//   3. adds the published histograms of the chunks before its own, which
+//      gives, per expert, the slots that precede its own range; ranks its own
+//      slots in order (equal-key lane masks), which gives each slot's packed
+//      row -- the global exclusive count of its expert (§1.2, §3.2) -- and
+//      writes combine_idx and src_info for the tokens whose first piece it
+//      holds (the CTA holding the last token writes recv_count);
+//   4. arrives at a grid barrier (workspace counter) and issues the k bulk
+//      stores of every unit from warps 0..14, while warp 15 waits for the
+//      barrier and then, for the experts e = cta + n * grid, derives
+//      layout_range from the sources of their rows (sorted by token, so each
+//      rank is one run) and (FP8) writes their column-major scales, coalesced
+//      along rows, as the bulk stores drain.
+// All CTAs are resident at once (one per SM, grid = SM count), so the waits
+// on other CTAs (chunk flags, the barrier) end; every wait is bounded anyway
+// and gives up with EP_ERR_TIMEOUT.
 
-// Low-latency scatter of a batch whose source rows fit in the CTAs' shared
-// memory (decode sizes).  Everything that does not need the layout is done
-// while the layout kernel still runs: each warp bulk-loads ALL its units'
-// bf16 pieces at once, one slot and one mbarrier per unit, and (FP8)
-// quantises every piece in place (a lane reads its 32 bytes, the warp syncs,
-// then the lane writes its 16 E4M3 bytes over the front of the slot).  Only
-// then does it wait for the layout (griddepcontrol.wait), fetch all its
-// destinations at once and issue the bulk stores back to back, so the store
-// stream starts the moment the layout is known and never waits on a load.
+constexpr int kFusedWarps = 16;
+constexpr int kFusedMaxPerWarp = 8;      // units per store warp
+constexpr int kFusedPiece = 1024;        // channels per unit
+constexpr int kRankWarps = 8;            // warps that rank a CTA's own slots
+constexpr int kRankIdsPerLane = 4;
+constexpr int kMaxOwnIds = kRankWarps * kWarp * kRankIdsPerLane;
+constexpr int kFusedChunkIds = 1024;     // ids per published histogram
+constexpr int kFusedBarBytes = kFusedWarps * kFusedMaxPerWarp * 8;
+constexpr size_t kFusedSmemCap = 225 * 1024;
+constexpr int kCtlArrive = 8;            // workspace control words of this kernel
+constexpr int kCtlExit = 9;
+constexpr int kCtlEpoch = 10;
+
+// Wait (bounded, kWaitNs) until a grid counter reaches n; false on timeout.
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t n) {
+  if (ld_acquire_u32(ctr) >= n) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_u32(ctr) < n) {
+    __nanosleep(64);
+    if (globaltimer_ns() - t0 > kWaitNs) return false;
+  }
+  return true;
+}
+
+struct FusedParams {
+  const uint8_t* x;
+  const int64_t* topk_idx;
+  int R, T_r, H, E, k;
+  int32_t T;
+  int32_t n_ids;             // T * k
+  int64_t seg_rows;          // R * max_tokens_per_rank (rows per expert)
+  uint8_t* recv_x;           // packed [E][seg_rows][row bytes]
+  void* scales;              // packed column-major [E][H/128][seg_rows]
+  int32_t* src_info;         // [E][seg_rows]
+  int64_t* layout_range;     // [E][R]
+  int32_t* recv_count;       // [E]
+  int32_t* combine_idx;      // [T][k]
+  uint8_t* scale_rows;       // [T][scale_row_bytes] staged per-token scales
+  int scale_row_bytes;
+  uint32_t* ctl;             // workspace control words
+  uint64_t* chunk_hist;      // [num_chunks][E] (launch tag << 32) | count
+  int num_chunks;
+  int32_t* status;
+  // geometry
+  int Hp, P;
+  int32_t n_units;
+  uint32_t slot_bytes;       // one bf16 piece, 128-byte multiple
+  uint32_t slot_area;        // bytes of the CTA's slots
+  int own_cap;               // own-id capacity (multiple of 32)
+  int nA;                    // experts per CTA (ceil(E / grid))
+  int nbits;
+};
+
 template <int kMode>
-__global__ void __launch_bounds__(kStagedWarps * kWarp, 1) k_ll_scatter_staged(ScatterParams p) {
+__global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr bool kFp8 = kMode != EP_FP8_NONE;
   constexpr int kEs = kMode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  if (kFp8) pdl_launch_dependents();   // the scale-column pass may launch
-  const int32_t U = (int32_t)p.n_units;
-  const int32_t u0 = (int32_t)((int64_t)U * blockIdx.x / gridDim.x);
-  const int32_t u1 = (int32_t)((int64_t)U * (blockIdx.x + 1) / gridDim.x);
-  const int32_t nm = warp < u1 - u0 ? (u1 - u0 - warp + kStagedWarps - 1) / kStagedWarps : 0;
-  const uint32_t slot_bytes = p.in_bytes;   // one bf16 piece
-  uint8_t* slots = smem;                    // [units of this CTA][slot_bytes]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)p.warp_smem) + warp * kStagedMaxPerWarp;
-  const int64_t row_bytes = kFp8 ? (int64_t)p.H : (int64_t)p.H * 2;
-  auto unit_slot = [&](int32_t m) { return slots + (size_t)(warp + m * kStagedWarps) * slot_bytes; };
+  constexpr int kThreads = kFusedWarps * kWarp;
+  __shared__ uint32_t s_epoch;
+  __shared__ int s_ok;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int grid = (int)gridDim.x;
+  const int cta = (int)blockIdx.x;
+
+  const int32_t U = p.n_units;
+  const int32_t u0 = (int32_t)((int64_t)U * cta / grid);
+  const int32_t u1 = (int32_t)((int64_t)U * (cta + 1) / grid);
+  const int32_t nm = warp < u1 - u0 ? (u1 - u0 - warp + kFusedWarps - 1) / kFusedWarps : 0;
+  uint8_t* slots = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.slot_area) + warp * kFusedMaxPerWarp;
+  int32_t* s_P = reinterpret_cast<int32_t*>(smem + p.slot_area + kFusedBarBytes);   // [E]
+  int32_t* s_cnt = s_P + p.E;                    // [kRankWarps][E]
+  int32_t* s_H = s_cnt + kRankWarps * p.E;       // [E] histogram of chunk `cta`
+  int32_t* s_own = s_H + p.E;                    // [own_cap] own ids
+  int32_t* s_f = s_own + p.own_cap;              // [own_cap] their packed rows
+  int32_t* s_lo = s_f + p.own_cap;               // [nA][R + 1] first row of every rank
+  auto unit_slot = [&](int32_t m) { return slots + (size_t)(warp + m * kFusedWarps) * p.slot_bytes; };
   auto unit_of = [&](int32_t m, int32_t* g, int* pc) {
-    const int32_t u = u0 + warp + m * kStagedWarps;
+    const int32_t u = u0 + warp + m * kFusedWarps;
     *g = u / p.P;
     *pc = u - *g * p.P;
   };
 
-  // ---- 1. all source pieces in flight
+  // own token range [ga, gb) and the ids this CTA reads
+  const int32_t ga = u0 / p.P;
+  const int32_t gb = u1 > u0 ? (u1 - 1) / p.P + 1 : ga;
+  const int32_t own_lo = ga * p.k;
+  const int32_t own_hi = gb * p.k;
+  const int32_t own_n = own_hi - own_lo;
+  const int32_t J = own_lo / kFusedChunkIds;        // chunks wholly before the own range
+  const int32_t scan_lo = J * kFusedChunkIds;       // counted here: [scan_lo, own_hi)
+  const bool chunk_cta = cta < p.num_chunks;
+  const int32_t ch_lo = cta * kFusedChunkIds;
+  const int32_t ch_hi = min(ch_lo + kFusedChunkIds, p.n_ids);
+  const int64_t last_first = (int64_t)(p.T - 1) * p.P;
+  const bool totals = last_first >= u0 && last_first < u1;   // sees every id: writes recv_count
+
+  // ---- 0. the ids: they are on the critical path, so they go out before any
+  //      bulk load of x (which would queue them behind ~30 MB of reads)
+  constexpr int kScanPairs = 2;                     // 16-byte id loads per thread per pass
+  longlong2 vc = make_longlong2(-1, -1);
+  longlong2 vs[kScanPairs];
+  {
+    const int32_t q = ch_lo + 2 * tid;
+    if (chunk_cta && q + 1 < ch_hi) vc = ld_nc_i64x2(p.topk_idx + q);
+    else if (chunk_cta && q < ch_hi) vc.x = __ldg(p.topk_idx + q);
+  }
+  auto load_scan = [&](int32_t base) {
+#pragma unroll
+    for (int u = 0; u < kScanPairs; ++u) {
+      const int32_t q = base + 2 * (tid + u * kThreads);
+      vs[u] = make_longlong2(-1, -1);
+      if (q + 1 < own_hi) vs[u] = ld_nc_i64x2(p.topk_idx + q);
+      else if (q < own_hi) vs[u].x = __ldg(p.topk_idx + q);
+    }
+  };
+  load_scan(scan_lo);
+  for (int i = tid; i < (2 + kRankWarps) * p.E; i += kThreads) s_P[i] = 0;   // s_P, s_cnt, s_H
+  if (tid == 0) s_epoch = ld_relaxed_u32(&p.ctl[kCtlEpoch]);
+  __syncthreads();
+  const uint32_t tag = s_epoch + 1u;
+
+  // ---- 1. the chunk histogram (published), the partial prefix and own ids
+  {
+    bool bad = false;
+    auto valid = [&](int64_t id) {
+      if (id >= 0 && id < p.E) return (int)id;
+      bad |= (id != -1);
+      return -1;
+    };
+    if (chunk_cta) {
+      const int e0 = valid(vc.x), e1 = valid(vc.y);
+      if (e0 >= 0) atomicAdd(&s_H[e0], 1);
+      if (e1 >= 0) atomicAdd(&s_H[e1], 1);
+    }
+    auto count = [&](int32_t q, int64_t id) {
+      const int e = valid(id);
+      if (q < own_lo) {
+        if (e >= 0) atomicAdd(&s_P[e], 1);
+      } else {
+        s_own[q - own_lo] = e;
+      }
+    };
+    for (int32_t base = scan_lo; base < own_hi; base += 2 * kThreads * kScanPairs) {
+      if (base > scan_lo) load_scan(base);
+#pragma unroll
+      for (int u = 0; u < kScanPairs; ++u) {
+        const int32_t q = base + 2 * (tid + u * kThreads);
+        if (q < own_hi) count(q, vs[u].x);
+        if (q + 1 < own_hi) count(q + 1, vs[u].y);
+      }
+    }
+    if (bad) set_status(p.status, EP_ERR_INVALID_ARG);
+  }
+  __syncthreads();
+  if (chunk_cta)   // tagged words: a reader sees the old word or the whole new one
+    for (int e = tid; e < p.E; e += kThreads)
+      st_relaxed_u64(&p.chunk_hist[(size_t)cta * p.E + e], ((uint64_t)tag << 32) | (uint32_t)s_H[e]);
+  if (tid == 0) s_ok = 1;
+  __syncthreads();
+
+  // ---- 2. prefix of the chunks before the own range (their tagged words,
+  //      all loads of a pass in flight, a word re-read until its tag is this
+  //      launch's), then the own ranks
+  {
+    constexpr int kHistLoads = 8;
+    const int32_t n = J * p.E;
+    for (int32_t i0 = 0; i0 < n; i0 += kThreads * kHistLoads) {
+      uint64_t w[kHistLoads];
+#pragma unroll
+      for (int u = 0; u < kHistLoads; ++u) {
+        const int32_t i = i0 + u * kThreads + tid;
+        w[u] = i < n ? ld_relaxed_u64(&p.chunk_hist[i]) : ((uint64_t)tag << 32);
+      }
+#pragma unroll
+      for (int u = 0; u < kHistLoads; ++u) {
+        const int32_t i = i0 + u * kThreads + tid;
+        if ((uint32_t)(w[u] >> 32) != tag) {
+          const uint64_t t0 = globaltimer_ns();
+          do {
+            __nanosleep(32);
+            w[u] = ld_relaxed_u64(&p.chunk_hist[i]);
+            if (globaltimer_ns() - t0 > kWaitNs) {
+              set_status(p.status, EP_ERR_TIMEOUT);
+              s_ok = 0;
+              w[u] = (uint64_t)tag << 32;
+            }
+          } while ((uint32_t)(w[u] >> 32) != tag);
+        }
+        const int32_t c = (int32_t)(uint32_t)w[u];
+        if (c != 0) atomicAdd(&s_P[i % p.E], c);
+      }
+    }
+  }
+  __syncthreads();
+  const int per = ((own_n + kRankWarps * kWarp - 1) / (kRankWarps * kWarp)) * kWarp;
+  int my_rank[kRankIdsPerLane];
+  if (warp < kRankWarps) {
+#pragma unroll
+    for (int u = 0; u < kRankIdsPerLane; ++u) {
+      my_rank[u] = 0;
+      if (u * kWarp < per) {
+        const int q = warp * per + u * kWarp + lane;
+        const int e = q < own_n ? s_own[q] : -1;
+        const uint32_t peers = peers_mask(e, p.nbits);
+        int r = 0;
+        if (e >= 0) r = s_cnt[warp * p.E + e] + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (e >= 0 && (__ffs(peers) - 1) == lane) s_cnt[warp * p.E + e] += __popc(peers);
+        __syncwarp();
+        my_rank[u] = r;
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < p.E; e += kThreads) {   // per-warp counts -> warp starts
+    int run = s_P[e];
+#pragma unroll
+    for (int w = 0; w < kRankWarps; ++w) {
+      const int c = s_cnt[w * p.E + e];
+      s_cnt[w * p.E + e] = run;
+      run += c;
+    }
+    if (totals) p.recv_count[e] = run;
+  }
+  __syncthreads();
+  if (warp < kRankWarps) {
+#pragma unroll
+    for (int u = 0; u < kRankIdsPerLane; ++u) {
+      if (u * kWarp < per) {
+        const int q = warp * per + u * kWarp + lane;
+        if (q < own_n) {
+          const int e = s_own[q];
+          int32_t f = -1;
+          if (e >= 0 && s_ok) {
+            const int64_t row = (int64_t)s_cnt[warp * p.E + e] + my_rank[u];
+            if (row < p.seg_rows) f = (int32_t)((int64_t)e * p.seg_rows + row);
+            else set_status(p.status, EP_ERR_CAPACITY);
+          }
+          s_f[q] = f;
+          const int32_t g = ga + q / p.k;
+          if ((int64_t)g * p.P >= u0) {   // this CTA holds the token's first piece
+            p.combine_idx[own_lo + q] = f;
+            if (f >= 0) p.src_info[f] = g;
+          }
+        }
+      }
+    }
+  }
+  // every source piece of this CTA in flight, only now: a read issued while
+  // ~30 MB of bulk loads are queued waits behind them, and the steps above
+  // are one chain of such reads
   if (nm > 0 && lane == 0) {
     for (int32_t m = 0; m < nm; ++m) mbar_init(&bars[m], 1);
     fence_barrier_init();
@@ -489,25 +737,27 @@ __global__ void __launch_bounds__(kStagedWarps * kWarp, 1) k_ll_scatter_staged(S
       tma_load_1d(unit_slot(m), p.x + (int64_t)g * p.H * 2 + (int64_t)pc * p.Hp * 2, bytes, &bars[m]);
     }
   }
-  __syncwarp();
-  bool ok_all = true;
+  __syncthreads();
+
+  // ---- 3. per unit: wait for the piece, quantise it in place (staging the
+  //      token's scales row-major), issue its k bulk stores
+  const int64_t row_bytes = kFp8 ? (int64_t)p.H : (int64_t)p.H * 2;
   for (int32_t m = 0; m < nm; ++m) {
     const bool landed = mbar_wait_bounded(&bars[m], 0);
     if (!__all_sync(0xffffffffu, landed)) {
       set_status(p.status, EP_ERR_TIMEOUT);
-      ok_all = false;
       if (lane == 0)   // wait (bounded) for what is still in flight
         for (int32_t r = m; r < nm; ++r) mbar_wait_bounded(&bars[r], 0);
       break;
     }
-    if (kFp8) {   // ---- 2. quantise in place
-      int32_t g;
-      int pc;
-      unit_of(m, &g, &pc);
-      const int hc = min(p.Hp, p.H - pc * p.Hp);
-      uint8_t* sl = unit_slot(m);
+    int32_t g;
+    int pc;
+    unit_of(m, &g, &pc);
+    const int hc = min(p.Hp, p.H - pc * p.Hp);
+    uint8_t* sl = unit_slot(m);
+    if (kFp8) {
       uint8_t* srow = p.scale_rows + (int64_t)g * p.scale_row_bytes;
-      constexpr int kSegs = kStagedPiece / 512;
+      constexpr int kSegs = kFusedPiece / 512;
       uint4 a[kSegs], b[kSegs];
 #pragma unroll
       for (int sg = 0; sg < kSegs; ++sg) {
@@ -535,105 +785,176 @@ __global__ void __launch_bounds__(kStagedWarps * kWarp, 1) k_ll_scatter_staged(S
           }
         }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
     }
-  }
-  if (kFp8) fence_proxy_async_smem();
-  __syncwarp();
-
-  // ---- 3. the layout is needed from here on
-  pdl_wait();
-  int32_t fm[kStagedMaxPerWarp];
-#pragma unroll
-  for (int m = 0; m < kStagedMaxPerWarp; ++m) {
-    fm[m] = -1;
-    if (m < nm && lane < p.k) {
-      int32_t g;
-      int pc;
-      unit_of(m, &g, &pc);
-      int32_t f = p.combine_idx[(int64_t)g * p.k + lane];
-      if (f < -1 || (int64_t)f >= p.n_rows) {
-        set_status(p.status, EP_ERR_INVALID_ARG);
-        f = -1;
-      }
-      fm[m] = f;
-    }
-  }
-  if (ok_all) {
-#pragma unroll
-    for (int m = 0; m < kStagedMaxPerWarp; ++m) {
-      if (m < nm) {
-        int32_t g;
-        int pc;
-        unit_of(m, &g, &pc);
-        const int hc = min(p.Hp, p.H - pc * p.Hp);
+    if (lane < p.k) {
+      const int32_t f = s_f[(g - ga) * p.k + lane];
+      if (f >= 0) {
         const int64_t col = (int64_t)pc * p.Hp * (kFp8 ? 1 : 2);
-        const uint32_t bytes = (uint32_t)hc * (kFp8 ? 1u : 2u);
-        for (int j = 0; j < p.k; ++j) {
-          const int32_t f = __shfl_sync(0xffffffffu, fm[m], j);
-          if (lane == 0 && f >= 0) tma_store_1d(p.recv_x + f * row_bytes + col, unit_slot(m), bytes);
+        tma_store_1d(p.recv_x + f * row_bytes + col, sl, (uint32_t)hc * (kFp8 ? 1u : 2u));
+      }
+      tma_commit();
+    }
+  }
+
+  // ---- 4. grid barrier: every CTA has written its src_info and staged scales
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t a = atomicAdd(&p.ctl[kCtlArrive], 1u);
+    int good = 1;
+    if (a >= (uint32_t)grid) {   // workspace not cleaned
+      set_status(p.status, EP_ERR_STATE);
+      good = 0;
+    }
+    if (good && !wait_count(&p.ctl[kCtlArrive], (uint32_t)grid)) {
+      set_status(p.status, EP_ERR_TIMEOUT);
+      good = 0;
+    }
+    __threadfence();
+    s_ok = good;
+  }
+  __syncthreads();
+
+  // ---- 5. this CTA's experts e = cta + a * grid: layout_range from the
+  //      sources of their rows (sorted by token, so each rank is one run) and
+  //      (FP8) their column-major scales.  One item per (row, 16-byte scale
+  //      group), spread over all threads, every load of a pass in flight at
+  //      once: the bulk stores are still draining and every round trip is slow.
+  if (s_ok) {
+    int32_t* s_rows = s_P;   // [nA] rows per own expert (s_P is free once the ranks exist)
+    if (tid < p.nA) {
+      const int e = cta + tid * grid;
+      s_rows[tid] = e < p.E ? (int32_t)min((int64_t)max(ld_cg_i32(&p.recv_count[e]), 0), p.seg_rows) : 0;
+    }
+    __syncthreads();
+    int32_t total = 0;
+    for (int a = 0; a < p.nA; ++a) total += s_rows[a];
+    const int R1 = p.R + 1;
+    for (int a = 0; a < p.nA; ++a)   // experts without rows: every rank starts at 0
+      if (s_rows[a] == 0)
+        for (int i = tid; i < R1; i += kThreads) s_lo[a * R1 + i] = 0;
+    const int ngrp = kFp8 ? p.scale_row_bytes / 16 : 1;
+    const int nb = p.H / kFp8Block;
+    const int32_t items = total * ngrp;
+    for (int32_t it = tid; it < items; it += kThreads) {
+      const int grp = it % ngrp;
+      int32_t f = it / ngrp;
+      int a = 0;
+      while (a < p.nA - 1 && f >= s_rows[a]) f -= s_rows[a++];
+      const int32_t row = f;
+      const int32_t cnt = s_rows[a];
+      const int e = cta + a * grid;
+      const int32_t* src = p.src_info + (int64_t)e * p.seg_rows;
+      const int32_t s = ld_cg_i32(&src[row]);
+      const int32_t s_prev = (grp == 0 && row > 0) ? ld_cg_i32(&src[row - 1]) : -1;
+      uint4 w4 = make_uint4(0, 0, 0, 0);
+      const bool have = kFp8 && s >= 0 && s < p.T;
+      if (have) w4 = ld_cg_v4(p.scale_rows + (int64_t)s * p.scale_row_bytes + grp * 16);
+      if (grp == 0) {
+        // ranks (rank of row - 1, rank of row] start at this row; the last
+        // row also closes the ranks after its own
+        int32_t* lo = s_lo + a * R1;
+        const int lo_rank = row == 0 ? 0 : max(s_prev, 0) / p.T_r + 1;
+        const int cur_rank = max(s, 0) / p.T_r;
+        for (int i = max(lo_rank, 0); i <= min(cur_rank, p.R); ++i) lo[i] = row;
+        if (row == cnt - 1)
+          for (int i = max(cur_rank + 1, 0); i <= p.R; ++i) lo[i] = cnt;
+      }
+      if (have) {
+        constexpr int kPer16 = 16 / kEs;
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int t = 0; t < kPer16; ++t) {
+          const int b = grp * kPer16 + t;
+          if (b < nb) {
+            const int64_t o = ((int64_t)e * nb + b) * p.seg_rows + row;
+            if (kEs == 4) static_cast<uint32_t*>(p.scales)[o] = w[t];
+            else static_cast<uint8_t*>(p.scales)[o] = (uint8_t)(w[t >> 2] >> (8 * (t & 3)));
+          }
         }
       }
     }
+    __syncthreads();
+    for (int i = tid; i < p.nA * p.R; i += kThreads) {
+      const int a = i / p.R;
+      const int r = i - a * p.R;
+      const int e = cta + a * grid;
+      if (e < p.E)
+        p.layout_range[(size_t)e * p.R + r] =
+            ((int64_t)s_lo[a * R1 + r] << 32) | (int64_t)(s_lo[a * R1 + r + 1] - s_lo[a * R1 + r]);
+    }
   }
-  if (lane == 0 && nm > 0) {
-    tma_commit();
-    tma_wait_all();
+  __syncthreads();
+  if (tid == 0) {   // the last CTA out resets the barrier and moves the epoch on
+    const uint32_t d = atomicAdd(&p.ctl[kCtlExit], 1u);
+    if (d == (uint32_t)grid - 1) {
+      p.ctl[kCtlArrive] = 0;
+      p.ctl[kCtlExit] = 0;
+      p.ctl[kCtlEpoch] = s_epoch + 1u;
+    }
   }
+  tma_wait_all();   // the bulk stores have read their slots before the CTA leaves
 }
 
-// Geometry of the staged path, or false when the batch does not fit.
-static size_t staged_smem(const ScatterParams& p) {
-  return (size_t)p.warp_smem + (size_t)kStagedWarps * kStagedMaxPerWarp * sizeof(uint64_t);
+static size_t fused_smem(const FusedParams& p) {
+  const size_t tables = (size_t)p.E * (2 + kRankWarps) + 2 * (size_t)p.own_cap +
+                        (size_t)p.nA * (p.R + 1);
+  return (size_t)p.slot_area + kFusedBarBytes + tables * sizeof(int32_t);
 }
 
-static bool plan_staged(ScatterParams& p) {
-  const int hp = std::min(p.H, kStagedPiece);
+// Workspace bytes of the fused path's chunk histograms (after the FP8 staging).
+static size_t fused_region_bytes(int R, int T_r, int k, int E) {
+  const int64_t chunks = ((int64_t)R * T_r * k + kFusedChunkIds - 1) / kFusedChunkIds;
+  return (size_t)((chunks * E * 8 + 255) / 256 * 256);
+}
+
+// Geometry of the fused path, or false when the batch does not fit it.
+static bool plan_fused(FusedParams& p, int grid) {
+  if ((int64_t)p.T * p.k >= INT32_MAX || p.T == 0) return false;
+  const int hp = std::min(p.H, kFusedPiece);
   p.Hp = hp;
   p.P = (p.H + hp - 1) / hp;
-  p.n_units = p.T * p.P;
-  const int grid = ep_host::num_sms();
-  const int64_t per_cta = (p.n_units + grid - 1) / grid;
-  if (per_cta > (int64_t)kStagedWarps * kStagedMaxPerWarp) return false;
-  p.in_bytes = round128((uint32_t)hp * 2u);            // one slot per unit
-  p.warp_smem = (uint32_t)(per_cta * p.in_bytes);      // slot area of the CTA
-  p.warps_per_cta = kStagedWarps;
-  return staged_smem(p) <= kScatterSmemBudget;
+  const int64_t units = (int64_t)p.T * p.P;
+  const int64_t per_cta = (units + grid - 1) / grid;
+  if (per_cta > (int64_t)kFusedWarps * kFusedMaxPerWarp) return false;
+  p.n_units = (int32_t)units;
+  p.slot_bytes = round128((uint32_t)hp * 2u);
+  p.slot_area = (uint32_t)(per_cta * p.slot_bytes);
+  const int64_t own_tokens = (per_cta + p.P - 1) / p.P + 1;
+  const int64_t own = (own_tokens * p.k + kWarp - 1) / kWarp * kWarp;
+  if (own > kMaxOwnIds) return false;
+  p.own_cap = (int)own;
+  p.num_chunks = (int)(((int64_t)p.T * p.k + kFusedChunkIds - 1) / kFusedChunkIds);
+  if (p.num_chunks > grid) return false;
+  p.nA = (p.E + grid - 1) / grid;
+  if (p.nA > kFusedWarps * kWarp) return false;
+  p.nbits = key_bits(p.E);
+  return fused_smem(p) <= kFusedSmemCap;
 }
 
 template <int kMode>
-static int launch_ll_staged_t(ScatterParams p, cudaStream_t stream) {
+static int launch_fused_t(const FusedParams& p, int grid, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(k_ll_scatter_staged<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kScatterSmemBudget + 1024) != cudaSuccess) {
+    if (cudaFuncSetAttribute(k_ll_fused<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFusedSmemCap) != cudaSuccess) {
       cudaGetLastError();
       return EP_ERR_CUDA;
     }
     attr_set = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ep_host::num_sms());
-  cfg.blockDim = dim3(kStagedWarps * kWarp);
-  cfg.dynamicSmemBytes = staged_smem(p);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, k_ll_scatter_staged<kMode>, p) != cudaSuccess) {
-    cudaGetLastError();
-    return EP_ERR_CUDA;
-  }
+  k_ll_fused<kMode><<<grid, kFusedWarps * kWarp, fused_smem(p), stream>>>(p);
   ep_host::count_launch();
   return ep_host::check_launch();
 }
 
-static int launch_ll_staged(const ScatterParams& p, int fp8_mode, cudaStream_t stream) {
+static int launch_fused(const FusedParams& p, int fp8_mode, int grid, cudaStream_t stream) {
   switch (fp8_mode) {
-    case EP_FP8_NONE: return launch_ll_staged_t<EP_FP8_NONE>(p, stream);
-    case EP_FP8_E4M3_F32_SCALE: return launch_ll_staged_t<EP_FP8_E4M3_F32_SCALE>(p, stream);
-    case EP_FP8_E4M3_UE8M0: return launch_ll_staged_t<EP_FP8_E4M3_UE8M0>(p, stream);
+    case EP_FP8_NONE: return launch_fused_t<EP_FP8_NONE>(p, grid, stream);
+    case EP_FP8_E4M3_F32_SCALE: return launch_fused_t<EP_FP8_E4M3_F32_SCALE>(p, grid, stream);
+    case EP_FP8_E4M3_UE8M0: return launch_fused_t<EP_FP8_E4M3_UE8M0>(p, grid, stream);
   }
   return EP_ERR_INVALID_ARG;
 }
@@ -828,18 +1149,26 @@ static int check_common(int R, int T_r, int H, int E, int k, int fp8_mode) {
   return EP_OK;
 }
 
-// Staged per-token scales live after the layout kernel's region of the
-// workspace (the two never alias).
+// Workspace: [layout kernel region][staged per-token FP8 scales][fused-path
+// chunk flags and histograms]; the three never alias.
+static size_t staging_bytes(int R, int T_r, int H) {
+  return ((size_t)R * T_r * scale_row_bytes(H, 4) + 255) / 256 * 256;
+}
+
 static uint8_t* scale_staging(void* ws, int R, int T_r, int k, int E) {
   return static_cast<uint8_t*>(ws) + layout_region_bytes(R, T_r, k, E);
+}
+
+static uint8_t* fused_region(void* ws, int R, int T_r, int k, int E, int H) {
+  return scale_staging(ws, R, T_r, k, E) + staging_bytes(R, T_r, H);
 }
 
 }  // namespace ep
 
 extern "C" size_t ep_workspace_size(int R, int T_r, int k, int E, int H) {
   if (R <= 0 || k <= 0 || k > ep::kMaxK || E <= 0 || T_r < 0 || H <= 0) return 0;
-  const size_t staging = (size_t)R * T_r * ep::scale_row_bytes(H, 4);
-  return ep::layout_region_bytes(R, T_r, k, E) + (staging + 255) / 256 * 256;
+  return ep::layout_region_bytes(R, T_r, k, E) + ep::staging_bytes(R, T_r, H) +
+         ep::fused_region_bytes(R, T_r, k, E);
 }
 
 extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t* slot_rank,
@@ -921,9 +1250,43 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
     return EP_ERR_INVALID_ARG;
   if (workspace_bytes < ep_workspace_size(R, T_r, k, E, H)) return EP_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int es = fp8_mode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
+  uint8_t* scale_rows = fp8 ? ep::scale_staging(workspace, R, T_r, k, E) : nullptr;
 
-  // multi-CTA look-back layout; the scatter follows as its programmatic
-  // dependent launch, the scale columns as the scatter's.
+  // decode-size batches: one fused launch (layout + scatter + scales)
+  const int grid = ep_host::num_sms();
+  if (ep_host::aligned16(topk_idx) && (int64_t)R * T_r * k < INT32_MAX) {
+    ep::FusedParams fp{};
+    fp.x = static_cast<const uint8_t*>(x);
+    fp.topk_idx = topk_idx;
+    fp.R = R;
+    fp.T_r = T_r;
+    fp.H = H;
+    fp.E = E;
+    fp.k = k;
+    fp.T = R * T_r;
+    fp.n_ids = fp.T * k;
+    fp.seg_rows = seg_rows;
+    fp.recv_x = static_cast<uint8_t*>(packed_recv_x);
+    fp.scales = packed_recv_scales;
+    fp.src_info = packed_recv_src_info;
+    fp.layout_range = layout_range;
+    fp.recv_count = recv_count;
+    fp.combine_idx = combine_idx;
+    fp.scale_rows = scale_rows;
+    fp.scale_row_bytes = fp8 ? ep::scale_row_bytes(H, es) : 0;
+    fp.ctl = static_cast<uint32_t*>(workspace);
+    uint8_t* fr = ep::fused_region(workspace, R, T_r, k, E, H);
+    const int64_t chunks = ((int64_t)R * T_r * k + ep::kFusedChunkIds - 1) / ep::kFusedChunkIds;
+    (void)chunks;
+    fp.chunk_hist = reinterpret_cast<uint64_t*>(fr);
+    fp.status = status;
+    if (ep::plan_fused(fp, grid))
+      return ep::launch_fused(fp, fp8_mode, grid, s);
+  }
+
+  // larger batches: multi-CTA look-back layout; the scatter follows as its
+  // programmatic dependent launch, the scale columns as the scatter's.
   ep::LayoutParams lp{};
   lp.topk_idx = topk_idx;
   lp.R = R;
@@ -953,17 +1316,14 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
   p.n_rows = (int64_t)E * seg_rows;
   p.recv_x = static_cast<uint8_t*>(packed_recv_x);
   p.combine_idx = combine_idx;
-  const int es = fp8_mode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
   if (fp8) {
-    p.scale_rows = ep::scale_staging(workspace, R, T_r, k, E);
+    p.scale_rows = scale_rows;
     p.scale_row_bytes = ep::scale_row_bytes(H, es);
   }
   p.status = status;
   p.n_pad_items = 0;
   if (p.T == 0) return EP_OK;
-  ep::ScatterParams ps = p;
-  rc = ep::plan_staged(ps) ? ep::launch_ll_staged(ps, fp8_mode, s)
-                           : ep::launch_scatter(p, fp8_mode, true, s);
+  rc = ep::launch_scatter(p, fp8_mode, true, s);
   if (rc != EP_OK || !fp8) return rc;
   ep::ScaleColParams sp{};
   sp.scale_rows = p.scale_rows;

@@ -68,8 +68,9 @@ extern "C" {
 /* Bytes of device workspace that ep_get_dispatch_layout, ep_dispatch and
  * ep_ll_dispatch need for problems up to (R, T_r, k, E, H); 0 for invalid
  * sizes.  The workspace holds the cross-block prefix (decoupled look-back)
- * state of the layout kernels and the per-token FP8 scales staged between
- * the scatter and the column-major scale pass.  It must be zeroed once with
+ * state of the layout kernels, the per-token FP8 scales staged between the
+ * scatter and the column-major scale pass, and the per-chunk histograms and
+ * barrier words of the single-launch low-latency path.  It must be zeroed once with
  * ep_clean_ll_buffer before its first use, after which every call leaves it
  * ready for the next.  Calls that share one workspace must be ordered on
  * one stream (overlapping calls race).  16-byte aligned. */
@@ -97,9 +98,8 @@ int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E
  * minus the workspace, which is replaced by a 4 MiB array inside libep
  * (held on every GPU that loads the library, until the process exits).
  *  - Returns EP_ERR_TOO_LARGE, launching nothing, when the problem's
- *    look-back state exceeds the array (ep_workspace_size(R, T_r, k, E, 8)
- *    minus the FP8 staging must fit in 4 MiB: e.g. R=8, T_r=16384, k=8,
- *    E=256 fits).
+ *    look-back state (the layout part of ep_workspace_size) exceeds the
+ *    array: e.g. R=8, T_r=16384, k=8, E=256 fits.
  *  - Allocates nothing: no cudaMalloc / cudaFree, no allocating library call.
  *  - Every call shares the one array and clears the part it uses first
  *    (stream-ordered); calls that overlap on the GPU race, so order them on
