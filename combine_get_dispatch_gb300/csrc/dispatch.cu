@@ -446,32 +446,37 @@ __global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterPar
 // scatter, FP8 quantisation and the column-major scales.  One CTA per SM;
 // the batch's (token, 1024-channel piece) units are split evenly over the
 // CTAs (a CTA's "own" tokens are those it holds a piece of), and every CTA
-//   0. loads the ids it needs and bulk-loads ALL its units' bf16 pieces at
-//      once (one shared-memory slot and one mbarrier per unit);
-//   1. CTA j < num_chunks histograms the j-th chunk of 1024 ids (in (rank,
-//      token, slot) order) and publishes it under a per-launch epoch; every
-//      CTA counts the ids between the start of the chunk holding its first
-//      own id and that id;
-//   2. (FP8) quantises each unit in place as it lands, staging the token's
-//      scales row-major in the workspace;
-//   3. adds the published histograms of the chunks before its own, which
-//      gives, per expert, the slots that precede its own range; ranks its own
-//      slots in order (equal-key lane masks), which gives each slot's packed
-//      row -- the global exclusive count of its expert (§1.2, §3.2) -- and
-//      writes combine_idx and src_info for the tokens whose first piece it
-//      holds (the CTA holding the last token writes recv_count);
-//   4. arrives at a grid barrier (workspace counter) and issues the k bulk
-//      stores of every unit from warps 0..14, while warp 15 waits for the
-//      barrier and then, for the experts e = cta + n * grid, derives
-//      layout_range from the sources of their rows (sorted by token, so each
-//      rank is one run) and (FP8) writes their column-major scales, coalesced
-//      along rows, as the bulk stores drain.
+//   0. loads the ids it needs: CTA j < num_chunks those of the j-th chunk of
+//      1024 ids (in (rank, token, slot) order), every CTA those from the
+//      start of the chunk holding its first own id to its last own id;
+//   1. histograms its chunk and publishes it as tagged 64-bit words (launch
+//      epoch in the high half: a reader needs no flag and no fence), counts
+//      its partial prefix and keeps its own ids;
+//   2. adds the histograms of the chunks before its own (re-reading a word
+//      until it carries this launch's tag), which gives, per expert, the
+//      slots that precede its own range; ranks its own slots in order
+//      (equal-key lane masks), which gives each slot's packed row -- the
+//      global exclusive count of its expert (§1.2, §3.2) -- and writes
+//      combine_idx and src_info for the tokens whose first piece it holds
+//      (the CTA holding the last token writes recv_count);
+//   3. only now bulk-loads its x pieces (a read issued while ~30 MB of bulk
+//      loads are queued waits behind them, and steps 0-2 are a chain of such
+//      reads); as each lands: bf16 -- issue its k bulk stores; FP8 --
+//      quantise it in place, staging the token's block scales row-major;
+//   4. arrives at a grid barrier (workspace counter).  FP8: warps 0..11 issue
+//      the k bulk stores of every unit while warps 12..15 wait for the
+//      barrier and write the per-expert outputs of the experts
+//      e = cta + n * grid as the stores drain: layout_range from the sources
+//      of their rows (sorted by token, so each rank is one run) and the
+//      column-major scales, coalesced along rows.  bf16: every warp waits
+//      and writes layout_range.
 // All CTAs are resident at once (one per SM, grid = SM count), so the waits
-// on other CTAs (chunk flags, the barrier) end; every wait is bounded anyway
+// on other CTAs (chunk words, the barrier) end; every wait is bounded anyway
 // and gives up with EP_ERR_TIMEOUT.
 
 constexpr int kFusedWarps = 16;
-constexpr int kFusedMaxPerWarp = 8;      // units per store warp
+constexpr int kStoreWarps = 12;          // FP8: warps issuing the bulk stores; the rest write the scales
+constexpr int kFusedMaxPerWarp = 8;      // units per warp
 constexpr int kFusedPiece = 1024;        // channels per unit
 constexpr int kRankWarps = 8;            // warps that rank a CTA's own slots
 constexpr int kRankIdsPerLane = 4;
@@ -523,6 +528,103 @@ struct FusedParams {
   int nbits;
 };
 
+// Per-expert outputs of the fused path for this CTA's experts e = cta + a * grid
+// (a < nA), by threads t < nt of a group that `sync` synchronises:
+// layout_range from the sources of their rows (sorted by token, so each
+// rank is one run) and (FP8) their column-major scales from the staged rows.
+// One item per (row, 16-byte scale group); a thread keeps kColBatch items'
+// loads in flight at once -- the bulk stores are draining and every round
+// trip is slow.
+template <bool kFp8, int kEs, class Sync>
+__device__ __forceinline__ void fused_expert_outputs(const FusedParams& p, int cta, int grid, int t,
+                                                     int nt, int32_t* s_rows, int32_t* s_lo, Sync sync) {
+  constexpr int kColBatch = 4;
+  if (t < p.nA) {
+    const int e = cta + t * grid;
+    s_rows[t] = e < p.E ? (int32_t)min((int64_t)max(ld_cg_i32(&p.recv_count[e]), 0), p.seg_rows) : 0;
+  }
+  sync();
+  int32_t total = 0;
+  for (int a = 0; a < p.nA; ++a) total += s_rows[a];
+  const int R1 = p.R + 1;
+  for (int a = 0; a < p.nA; ++a)   // experts without rows: every rank starts at 0
+    if (s_rows[a] == 0)
+      for (int i = t; i < R1; i += nt) s_lo[a * R1 + i] = 0;
+  const int ngrp = kFp8 ? p.scale_row_bytes / 16 : 1;
+  const int nb = p.H / kFp8Block;
+  const int32_t items = total * ngrp;
+  for (int32_t i0 = 0; i0 < items; i0 += nt * kColBatch) {
+    int a_of[kColBatch], grp[kColBatch];
+    int32_t row[kColBatch], s[kColBatch], s_prev[kColBatch];
+#pragma unroll
+    for (int u = 0; u < kColBatch; ++u) {
+      const int32_t it = i0 + u * nt + t;
+      a_of[u] = -1;
+      grp[u] = 0;
+      row[u] = 0;
+      s[u] = -1;
+      s_prev[u] = -1;
+      if (it < items) {
+        grp[u] = it % ngrp;
+        int32_t f = it / ngrp;
+        int a = 0;
+        while (a < p.nA - 1 && f >= s_rows[a]) f -= s_rows[a++];
+        a_of[u] = a;
+        row[u] = f;
+        const int32_t* src = p.src_info + (int64_t)(cta + a * grid) * p.seg_rows;
+        s[u] = ld_cg_i32(&src[f]);
+        if (grp[u] == 0 && f > 0) s_prev[u] = ld_cg_i32(&src[f - 1]);
+      }
+    }
+    uint4 w4[kColBatch];
+#pragma unroll
+    for (int u = 0; u < kColBatch; ++u) {
+      w4[u] = make_uint4(0, 0, 0, 0);
+      if (kFp8 && a_of[u] >= 0 && s[u] >= 0 && s[u] < p.T)
+        w4[u] = ld_cg_v4(p.scale_rows + (int64_t)s[u] * p.scale_row_bytes + grp[u] * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < kColBatch; ++u) {
+      if (a_of[u] < 0) continue;
+      const int a = a_of[u];
+      const int e = cta + a * grid;
+      if (grp[u] == 0) {
+        // ranks (rank of row - 1, rank of row] start at this row; the last
+        // row also closes the ranks after its own
+        int32_t* lo = s_lo + a * R1;
+        const int cnt = s_rows[a];
+        const int lo_rank = row[u] == 0 ? 0 : max(s_prev[u], 0) / p.T_r + 1;
+        const int cur_rank = max(s[u], 0) / p.T_r;
+        for (int i = max(lo_rank, 0); i <= min(cur_rank, p.R); ++i) lo[i] = row[u];
+        if (row[u] == cnt - 1)
+          for (int i = max(cur_rank + 1, 0); i <= p.R; ++i) lo[i] = cnt;
+      }
+      if (kFp8 && s[u] >= 0 && s[u] < p.T) {
+        constexpr int kPer16 = 16 / kEs;
+        const uint32_t w[4] = {w4[u].x, w4[u].y, w4[u].z, w4[u].w};
+#pragma unroll
+        for (int q = 0; q < kPer16; ++q) {
+          const int b = grp[u] * kPer16 + q;
+          if (b < nb) {
+            const int64_t o = ((int64_t)e * nb + b) * p.seg_rows + row[u];
+            if (kEs == 4) static_cast<uint32_t*>(p.scales)[o] = w[q];
+            else static_cast<uint8_t*>(p.scales)[o] = (uint8_t)(w[q >> 2] >> (8 * (q & 3)));
+          }
+        }
+      }
+    }
+  }
+  sync();
+  for (int i = t; i < p.nA * p.R; i += nt) {
+    const int a = i / p.R;
+    const int r = i - a * p.R;
+    const int e = cta + a * grid;
+    if (e < p.E)
+      p.layout_range[(size_t)e * p.R + r] =
+          ((int64_t)s_lo[a * R1 + r] << 32) | (int64_t)(s_lo[a * R1 + r + 1] - s_lo[a * R1 + r]);
+  }
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -530,7 +632,7 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   constexpr int kEs = kMode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
   constexpr int kThreads = kFusedWarps * kWarp;
   __shared__ uint32_t s_epoch;
-  __shared__ int s_ok;
+  __shared__ int s_ok, s_units_ok;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -591,7 +693,10 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   };
   load_scan(scan_lo);
   for (int i = tid; i < (2 + kRankWarps) * p.E; i += kThreads) s_P[i] = 0;   // s_P, s_cnt, s_H
-  if (tid == 0) s_epoch = ld_relaxed_u32(&p.ctl[kCtlEpoch]);
+  if (tid == 0) {
+    s_epoch = ld_relaxed_u32(&p.ctl[kCtlEpoch]);
+    s_units_ok = 1;
+  }
   __syncthreads();
   const uint32_t tag = s_epoch + 1u;
 
@@ -739,13 +844,14 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   }
   __syncthreads();
 
-  // ---- 3. per unit: wait for the piece, quantise it in place (staging the
-  //      token's scales row-major), issue its k bulk stores
+  // ---- 3. quantise (FP8) in place as the pieces land, staging each token's
+  //      scales row-major; bf16 units are stored as they land
   const int64_t row_bytes = kFp8 ? (int64_t)p.H : (int64_t)p.H * 2;
   for (int32_t m = 0; m < nm; ++m) {
     const bool landed = mbar_wait_bounded(&bars[m], 0);
     if (!__all_sync(0xffffffffu, landed)) {
       set_status(p.status, EP_ERR_TIMEOUT);
+      s_units_ok = 0;
       if (lane == 0)   // wait (bounded) for what is still in flight
         for (int32_t r = m; r < nm; ++r) mbar_wait_bounded(&bars[r], 0);
       break;
@@ -785,106 +891,60 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
           }
         }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
-    if (lane < p.k) {
+    } else if (lane < p.k) {
       const int32_t f = s_f[(g - ga) * p.k + lane];
-      if (f >= 0) {
-        const int64_t col = (int64_t)pc * p.Hp * (kFp8 ? 1 : 2);
-        tma_store_1d(p.recv_x + f * row_bytes + col, sl, (uint32_t)hc * (kFp8 ? 1u : 2u));
-      }
+      if (f >= 0)
+        tma_store_1d(p.recv_x + f * row_bytes + (int64_t)pc * p.Hp * 2, sl, (uint32_t)hc * 2u);
       tma_commit();
     }
   }
+  if (kFp8) fence_proxy_async_smem();   // the E4M3 pieces are read by bulk stores
+  __syncthreads();   // this CTA's src_info and staged scales are written
 
-  // ---- 4. grid barrier: every CTA has written its src_info and staged scales
-  __syncthreads();
+  // ---- 4. grid barrier, then the per-expert outputs: layout_range and (FP8)
+  //      the column-major scales of this CTA's experts e = cta + a * grid.
+  //      FP8: warps 0..kStoreWarps-1 issue the bulk stores of every unit
+  //      meanwhile, so the scale pass runs while the stores drain.
   if (tid == 0) {
     __threadfence();
-    const uint32_t a = atomicAdd(&p.ctl[kCtlArrive], 1u);
-    int good = 1;
-    if (a >= (uint32_t)grid) {   // workspace not cleaned
+    if (atomicAdd(&p.ctl[kCtlArrive], 1u) >= (uint32_t)grid) {   // workspace not cleaned
       set_status(p.status, EP_ERR_STATE);
-      good = 0;
+      s_ok = 0;
     }
-    if (good && !wait_count(&p.ctl[kCtlArrive], (uint32_t)grid)) {
-      set_status(p.status, EP_ERR_TIMEOUT);
-      good = 0;
-    }
-    __threadfence();
-    s_ok = good;
   }
-  __syncthreads();
-
-  // ---- 5. this CTA's experts e = cta + a * grid: layout_range from the
-  //      sources of their rows (sorted by token, so each rank is one run) and
-  //      (FP8) their column-major scales.  One item per (row, 16-byte scale
-  //      group), spread over all threads, every load of a pass in flight at
-  //      once: the bulk stores are still draining and every round trip is slow.
-  if (s_ok) {
-    int32_t* s_rows = s_P;   // [nA] rows per own expert (s_P is free once the ranks exist)
-    if (tid < p.nA) {
-      const int e = cta + tid * grid;
-      s_rows[tid] = e < p.E ? (int32_t)min((int64_t)max(ld_cg_i32(&p.recv_count[e]), 0), p.seg_rows) : 0;
-    }
-    __syncthreads();
-    int32_t total = 0;
-    for (int a = 0; a < p.nA; ++a) total += s_rows[a];
-    const int R1 = p.R + 1;
-    for (int a = 0; a < p.nA; ++a)   // experts without rows: every rank starts at 0
-      if (s_rows[a] == 0)
-        for (int i = tid; i < R1; i += kThreads) s_lo[a * R1 + i] = 0;
-    const int ngrp = kFp8 ? p.scale_row_bytes / 16 : 1;
-    const int nb = p.H / kFp8Block;
-    const int32_t items = total * ngrp;
-    for (int32_t it = tid; it < items; it += kThreads) {
-      const int grp = it % ngrp;
-      int32_t f = it / ngrp;
-      int a = 0;
-      while (a < p.nA - 1 && f >= s_rows[a]) f -= s_rows[a++];
-      const int32_t row = f;
-      const int32_t cnt = s_rows[a];
-      const int e = cta + a * grid;
-      const int32_t* src = p.src_info + (int64_t)e * p.seg_rows;
-      const int32_t s = ld_cg_i32(&src[row]);
-      const int32_t s_prev = (grp == 0 && row > 0) ? ld_cg_i32(&src[row - 1]) : -1;
-      uint4 w4 = make_uint4(0, 0, 0, 0);
-      const bool have = kFp8 && s >= 0 && s < p.T;
-      if (have) w4 = ld_cg_v4(p.scale_rows + (int64_t)s * p.scale_row_bytes + grp * 16);
-      if (grp == 0) {
-        // ranks (rank of row - 1, rank of row] start at this row; the last
-        // row also closes the ranks after its own
-        int32_t* lo = s_lo + a * R1;
-        const int lo_rank = row == 0 ? 0 : max(s_prev, 0) / p.T_r + 1;
-        const int cur_rank = max(s, 0) / p.T_r;
-        for (int i = max(lo_rank, 0); i <= min(cur_rank, p.R); ++i) lo[i] = row;
-        if (row == cnt - 1)
-          for (int i = max(cur_rank + 1, 0); i <= p.R; ++i) lo[i] = cnt;
-      }
-      if (have) {
-        constexpr int kPer16 = 16 / kEs;
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-        for (int t = 0; t < kPer16; ++t) {
-          const int b = grp * kPer16 + t;
-          if (b < nb) {
-            const int64_t o = ((int64_t)e * nb + b) * p.seg_rows + row;
-            if (kEs == 4) static_cast<uint32_t*>(p.scales)[o] = w[t];
-            else static_cast<uint8_t*>(p.scales)[o] = (uint8_t)(w[t >> 2] >> (8 * (t & 3)));
-          }
+  const int32_t n_own_units = u1 - u0;
+  if (kFp8 && warp < kStoreWarps) {
+    if (s_units_ok) {
+      for (int32_t q = warp; q < n_own_units; q += kStoreWarps) {
+        const int32_t u = u0 + q;
+        const int32_t g = u / p.P;
+        const int pc = u - g * p.P;
+        const int hc = min(p.Hp, p.H - pc * p.Hp);
+        if (lane < p.k) {
+          const int32_t f = s_f[(g - ga) * p.k + lane];
+          if (f >= 0)
+            tma_store_1d(p.recv_x + f * row_bytes + (int64_t)pc * p.Hp, slots + (size_t)q * p.slot_bytes,
+                         (uint32_t)hc);
+          tma_commit();
         }
       }
     }
-    __syncthreads();
-    for (int i = tid; i < p.nA * p.R; i += kThreads) {
-      const int a = i / p.R;
-      const int r = i - a * p.R;
-      const int e = cta + a * grid;
-      if (e < p.E)
-        p.layout_range[(size_t)e * p.R + r] =
-            ((int64_t)s_lo[a * R1 + r] << 32) | (int64_t)(s_lo[a * R1 + r + 1] - s_lo[a * R1 + r]);
+  } else {
+    const int t0 = kFp8 ? tid - kStoreWarps * kWarp : tid;
+    const int nt = kFp8 ? kThreads - kStoreWarps * kWarp : kThreads;
+    auto sync = [&]() {
+      if (kFp8) named_barrier_sync(1, kThreads - kStoreWarps * kWarp);
+      else __syncthreads();
+    };
+    if (t0 == 0) {
+      if (!wait_count(&p.ctl[kCtlArrive], (uint32_t)grid)) {
+        set_status(p.status, EP_ERR_TIMEOUT);
+        s_ok = 0;
+      }
+      __threadfence();
     }
+    sync();
+    if (s_ok) fused_expert_outputs<kFp8, kEs>(p, cta, grid, t0, nt, s_P, s_lo, sync);
   }
   __syncthreads();
   if (tid == 0) {   // the last CTA out resets the barrier and moves the epoch on

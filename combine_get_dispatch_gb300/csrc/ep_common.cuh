@@ -117,6 +117,11 @@ __host__ __device__ __forceinline__ int key_bits(int n) {
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Barrier `id` (1..15) among `n` threads (whole warps) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // 16-byte read-only streaming load (data not reused by this SM).
