@@ -134,3 +134,36 @@ def test_clean_ll_buffer_zeroes_counts_and_workspace():
     ep.ep_clean_ll_buffer(d["recv_count"], w.R, w.E, d["ws"])
     assert int(d["recv_count"].abs().sum()) == 0
     assert int(d["ws"].sum()) == 0
+
+
+def test_single_launch_path_reports_an_uncleaned_workspace():
+    """Host-made fault on the single-launch path (decode-size batches): the
+    workspace's grid-barrier word is left far past the CTA count, as a
+    workspace that was never cleaned might hold.  The call must finish,
+    report EP_ERR_STATE, and after ep_clean_ll_buffer the same workspace
+    must give the oracle's results again."""
+    w = synth.scaled(synth.WORKLOADS["tiny"], fp8_mode=2)
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    ws[32:36].view(torch.int32)[0] = 0x7FFFFF00      # barrier arrival word
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, 2, ws=ws)
+    torch.cuda.synchronize()
+    assert ep.ep_read_status(d["status"]) == ep.EP_ERR_STATE
+    ep.ep_clean_ll_buffer(d["recv_count"], w.R, w.E, ws)
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, 2, ws=ws)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_ll(w, x_host, idx, d, w.max_tokens_per_rank, 2)
+
+
+@pytest.mark.parametrize("fp8_mode", [0, 1, 2])
+def test_single_launch_path_repeated_calls_on_one_workspace(fp8_mode):
+    """The single-launch path moves its launch epoch on at every call; five
+    calls in a row on one workspace (different routings) must each match
+    the oracle."""
+    base = synth.scaled(synth.WORKLOADS["decode"], T_r=24, H=1024, fp8_mode=fp8_mode)
+    ws = ep.alloc_workspace(base.R, base.T_r, base.k, base.E, base.H)
+    for seed in range(5):
+        x_dev, x_host, idx_dev, idx, _, _ = inputs(base, seed=seed)
+        d = gpu_ll_dispatch(x_dev, idx_dev, base.E, base.max_tokens_per_rank, fp8_mode, ws=ws)
+        assert ep.ep_read_status(d["status"]) == ep.EP_OK
+        _compare_ll(base, x_host, idx, d, base.max_tokens_per_rank, fp8_mode)
