@@ -266,22 +266,31 @@ def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
     code = ep.ep_read_status(runner.status)
     if code != ep.EP_OK:
         raise RuntimeError(f"{runner.w.name}: kernel status {ep.error_string(code)}")
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    # the step as a user runs it: events only around it
+    outer = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(steps)]
     barrier(world, runner.dev)
     torch.cuda.synchronize()
     launches0 = ep.ep_launch_count()
     t_wall = time.perf_counter()
     for s in range(steps):
         flush.fill_(s & 0xFF)
-        e = evs[s]
-        e[4].record()
-        runner.step(e[:4])
-        e[5].record()
+        outer[s][0].record()
+        runner.step()
+        outer[s][1].record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
     barrier(world, runner.dev)
     launches = ep.ep_launch_count() - launches0
-    step_ms = [e[4].elapsed_time(e[5]) for e in evs]
+    step_ms = [a.elapsed_time(b) for a, b in outer]
+    # the same steps again with events between dispatch and combine (their
+    # split; the extra events cost the step a few microseconds)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        runner.step(evs[s])
+    torch.cuda.synchronize()
     disp_ms = [e[0].elapsed_time(e[1]) for e in evs]
     comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
     res = {"step_ms": statistics.mean(step_ms), "step_ms_min": min(step_ms),

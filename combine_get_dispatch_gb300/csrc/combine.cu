@@ -9,6 +9,10 @@
 // __floats2bfloat162_rn.  The same kernel serves the contiguous layout
 // (rows of [R, cap_rows]) and the packed layout (rows of [E, R*max]).
 //
+// Launched with programmatic dependent launch: it waits (griddepcontrol)
+// for the kernel before it -- the dispatch that wrote combine_idx -- to
+// complete, but its CTAs can be resident by then, which hides the launch.
+//
 // One warp handles one (token, 512-channel segment) item: every lane issues
 // all k row loads of its 2 x 16 bytes before the first fma (k*2 independent
 // 16-byte streaming loads in flight per lane), then reduces in registers and
@@ -35,6 +39,9 @@ struct CombineParams {
 template <int kU, int kK>
 __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineParams p) {
   constexpr int kSegC = kU * kWarp * 8;
+  // launched as a programmatic dependent: the CTAs may be resident before
+  // the kernel that wrote combine_idx (the dispatch) has finished
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCombineThreads) >> 5;
@@ -116,7 +123,20 @@ static int launch_combine_t(const CombineParams& p, cudaStream_t stream) {
   if (items == 0) return EP_OK;
   const int64_t want = (items + (kCombineThreads / kWarp) - 1) / (kCombineThreads / kWarp);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::num_sms() * 2));
-  k_combine<kU, kK><<<grid, kCombineThreads, 0, stream>>>(q);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_combine<kU, kK>, q) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
   ep_host::count_launch();
   return ep_host::check_launch();
 }

@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   constexpr int kEs = kMode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
   constexpr int kThreads = kFusedWarps * kWarp;
   __shared__ uint32_t s_epoch;
-  __shared__ int s_ok, s_units_ok;
+  __shared__ int s_ok, s_units_ok, s_passed;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -912,6 +912,9 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
       s_ok = 0;
     }
   }
+  // s_ok is final from here on: every thread that branches on it below (some
+  // of them before a named barrier) reads the same value
+  __syncthreads();
   const int32_t n_own_units = u1 - u0;
   if (kFp8 && warp < kStoreWarps) {
     if (s_units_ok) {
@@ -936,17 +939,16 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
       if (kFp8) named_barrier_sync(1, kThreads - kStoreWarps * kWarp);
       else __syncthreads();
     };
-    if (t0 == 0) {
-      if (!wait_count(&p.ctl[kCtlArrive], (uint32_t)grid)) {
-        set_status(p.status, EP_ERR_TIMEOUT);
-        s_ok = 0;
-      }
+    if (t0 == 0) {   // the group's leader alone writes s_passed; the group reads it after sync()
+      s_passed = wait_count(&p.ctl[kCtlArrive], (uint32_t)grid) ? 1 : 0;
+      if (!s_passed) set_status(p.status, EP_ERR_TIMEOUT);
       __threadfence();
     }
     sync();
-    if (s_ok) fused_expert_outputs<kFp8, kEs>(p, cta, grid, t0, nt, s_P, s_lo, sync);
+    if (s_ok && s_passed) fused_expert_outputs<kFp8, kEs>(p, cta, grid, t0, nt, s_P, s_lo, sync);
   }
   __syncthreads();
+  pdl_launch_dependents();   // a dependent combine may take its place as this drains
   if (tid == 0) {   // the last CTA out resets the barrier and moves the epoch on
     const uint32_t d = atomicAdd(&p.ctl[kCtlExit], 1u);
     if (d == (uint32_t)grid - 1) {
@@ -1030,58 +1032,122 @@ struct ScaleColParams {
   const int32_t* src_idx;      // token of every receive row, -1 = none (normal mode)
   const int32_t* recv_count;   // low-latency mode: rows per expert segment (src_idx
                                // is only defined below it)
+  const int64_t* psum;         // normal mode: [R][E_l + 1] segment starts
+  const int32_t* expert_total; // normal mode: [E] rows of every expert (unaligned)
+  int E, E_l;
   void* out;                   // column-major scales [segment][block][row]
 };
 
 constexpr int kScaleMaxGroups = 8;   // 16-byte groups of a staged scale row held at once
 
-// Flat over receive rows, one lane per row: a row holding a token gathers
-// that token's staged scales (16-byte loads, all issued before any store) and
-// writes them down its column entries -- consecutive lanes write consecutive
-// rows, so every store instruction is coalesced, and skewed routing (one
-// expert with most rows) spreads over all CTAs.
-template <bool kLL, int kEs>
-__global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColParams p) {
-  pdl_wait();   // the scatter's staged scales and row sources
+// One lane per receive row holding a token: it gathers that token's staged
+// scales (16-byte loads, all issued before any store) and writes them down
+// its column entries -- consecutive lanes write consecutive rows, so every
+// store instruction is coalesced.
+//   low-latency: one CTA per expert over its rows below recv_count;
+//   normal: a flat index over the valid rows of all expert segments (a
+//   segment's valid rows are its first expert_total[e] rows; the aligned
+//   rest and the capacity tail hold no token), mapped to (segment, row) by
+//   a binary search over the per-CTA prefix of the segment sizes, so skewed
+//   routing (one expert with most rows) spreads over all CTAs and padding
+//   rows cost nothing.
+template <int kEs>
+__device__ __forceinline__ void scale_row_to_columns(const ScaleColParams& p, int64_t seg,
+                                                     int64_t row, int64_t src) {
   constexpr int kPer16 = 16 / kEs;   // scale values per 16-byte group
   const int ngrp = p.row_bytes / 16;
-  // low-latency: grid (expert, row block) over the rows below recv_count;
-  // normal: flat over all rows (recv_src_idx is -1 where no token sits)
-  // low-latency: one CTA per expert over its rows below recv_count;
-  // normal: flat over all rows (recv_src_idx is -1 where no token sits)
-  const int64_t lim = kLL ? min((int64_t)max(__ldg(&p.recv_count[blockIdx.x]), 0), p.seg_rows) : 0;
-  int64_t f = kLL ? (int64_t)blockIdx.x * p.seg_rows + threadIdx.x
-                  : (int64_t)blockIdx.x * kScaleColThreads + threadIdx.x;
-  const int64_t f_end = kLL ? (int64_t)blockIdx.x * p.seg_rows + lim : p.n_rows;
-  const int64_t stride = kLL ? kScaleColThreads : (int64_t)gridDim.x * kScaleColThreads;
-  for (; f < f_end; f += stride) {
-    const int64_t seg = kLL ? (int64_t)blockIdx.x : f / p.seg_rows;
-    const int64_t row = f - seg * p.seg_rows;
-    bool valid = true;
-    const int64_t src = valid ? (int64_t)__ldg(&p.src_idx[f]) : -1;
-    valid = src >= 0 && src < p.T;
-    const uint8_t* srow = p.scale_rows + src * p.row_bytes;
-    for (int g0 = 0; g0 < ngrp; g0 += kScaleMaxGroups) {
-      uint4 v[kScaleMaxGroups];
+  const uint8_t* srow = p.scale_rows + src * p.row_bytes;
+  for (int g0 = 0; g0 < ngrp; g0 += kScaleMaxGroups) {
+    uint4 v[kScaleMaxGroups];
 #pragma unroll
-      for (int u = 0; u < kScaleMaxGroups; ++u)
-        v[u] = (valid && g0 + u < ngrp) ? __ldg(reinterpret_cast<const uint4*>(srow) + g0 + u)
-                                        : make_uint4(0, 0, 0, 0);
-      if (!valid) continue;
+    for (int u = 0; u < kScaleMaxGroups; ++u)
+      v[u] = g0 + u < ngrp ? __ldg(reinterpret_cast<const uint4*>(srow) + g0 + u)
+                           : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int u = 0; u < kScaleMaxGroups; ++u) {
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+    for (int u = 0; u < kScaleMaxGroups; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-        for (int t = 0; t < kPer16; ++t) {
-          const int b = (g0 + u) * kPer16 + t;
-          if (b < p.nb) {
-            const int64_t o = (seg * p.nb + b) * p.seg_rows + row;
-            if (kEs == 4) static_cast<uint32_t*>(p.out)[o] = w[t];
-            else static_cast<uint8_t*>(p.out)[o] = (uint8_t)(w[t >> 2] >> (8 * (t & 3)));
-          }
+      for (int t = 0; t < kPer16; ++t) {
+        const int b = (g0 + u) * kPer16 + t;
+        if (b < p.nb) {
+          const int64_t o = (seg * p.nb + b) * p.seg_rows + row;
+          if (kEs == 4) static_cast<uint32_t*>(p.out)[o] = w[t];
+          else static_cast<uint8_t*>(p.out)[o] = (uint8_t)(w[t >> 2] >> (8 * (t & 3)));
         }
       }
     }
+  }
+}
+
+template <bool kLL, int kEs>
+__global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColParams p) {
+  if (kLL) {
+    pdl_wait();   // the scatter's staged scales and row sources
+    const int64_t lim = min((int64_t)max(__ldg(&p.recv_count[blockIdx.x]), 0), p.seg_rows);
+    for (int64_t row = threadIdx.x; row < lim; row += kScaleColThreads) {
+      const int64_t f = (int64_t)blockIdx.x * p.seg_rows + row;
+      const int64_t src = __ldg(&p.src_idx[f]);
+      if (src >= 0 && src < p.T) scale_row_to_columns<kEs>(p, blockIdx.x, row, src);
+    }
+    return;
+  }
+  __shared__ int32_t s_base[kMaxE + 1];   // exclusive prefix of the valid rows per segment
+  __shared__ int32_t s_start[kMaxE];      // first row of every segment in its rank
+  __shared__ int32_t s_warp[kScaleColThreads / kWarp];
+  constexpr int kPer = (kMaxE + kScaleColThreads - 1) / kScaleColThreads;
+  const int tid = threadIdx.x;
+  int32_t cnt[kPer];
+  int32_t sum = 0;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid * kPer + u;
+    cnt[u] = 0;
+    if (e < p.E) {
+      const int r = e / p.E_l;
+      const int64_t start = __ldg(&p.psum[(size_t)r * (p.E_l + 1) + (e - r * p.E_l)]);
+      const int64_t room = max((int64_t)0, p.seg_rows - start);
+      cnt[u] = (int32_t)min((int64_t)max(__ldg(&p.expert_total[e]), 0), room);
+      s_start[e] = (int32_t)min(start, p.seg_rows);
+    }
+    sum += cnt[u];
+  }
+  // block-wide exclusive scan of the per-thread sums
+  const int lane = tid & 31, warp = tid >> 5;
+  int32_t incl = sum;
+#pragma unroll
+  for (int off = 1; off < kWarp; off <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == kWarp - 1) s_warp[warp] = incl;
+  __syncthreads();
+  int32_t before = 0;
+  for (int w = 0; w < warp; ++w) before += s_warp[w];
+  int32_t run = before + incl - sum;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid * kPer + u;
+    if (e < p.E) s_base[e] = run;
+    run += cnt[u];
+  }
+  if (tid == kScaleColThreads - 1) s_base[p.E] = run;   // the last thread holds the total
+  __syncthreads();
+  // the segment tables come from notify, complete before the scatter began;
+  // the staged scales and row sources need the scatter itself
+  pdl_wait();
+  const int32_t total = s_base[p.E];
+  for (int32_t f = blockIdx.x * kScaleColThreads + tid; f < total;
+       f += gridDim.x * kScaleColThreads) {
+    int lo = 0, hi = p.E;   // the segment e with s_base[e] <= f < s_base[e + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_base[mid] <= f) lo = mid;
+      else hi = mid;
+    }
+    const int r = lo / p.E_l;
+    const int64_t row = (int64_t)s_start[lo] + (f - s_base[lo]);
+    const int64_t src = __ldg(&p.src_idx[(int64_t)r * p.seg_rows + row]);
+    if (src >= 0 && src < p.T) scale_row_to_columns<kEs>(p, r, row, src);
   }
 }
 
@@ -1090,8 +1156,8 @@ static int launch_scale_columns_t(const ScaleColParams& p, cudaStream_t stream) 
   dim3 grid;
   if (kLL) {
     grid = dim3((unsigned)(p.n_rows / p.seg_rows));
-  } else {
-    const int64_t want = (p.n_rows + kScaleColThreads - 1) / kScaleColThreads;
+  } else {   // the valid rows are known only on the device: at most T * k
+    const int64_t want = (p.T * 16 + kScaleColThreads - 1) / kScaleColThreads;
     grid = dim3((unsigned)std::max<int64_t>(
         1, std::min<int64_t>(want, (int64_t)ep_host::num_sms() * 8)));
   }
@@ -1286,6 +1352,10 @@ extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t
   sp.seg_rows = cap_rows;
   sp.n_rows = (int64_t)R * cap_rows;
   sp.src_idx = recv_src_idx;
+  sp.psum = psum;
+  sp.expert_total = expert_prefix + (size_t)R * E;
+  sp.E = E;
+  sp.E_l = E / R;
   sp.out = recv_scales;
   return ep::launch_scale_columns(sp, false, fp8_mode, s);
 }
