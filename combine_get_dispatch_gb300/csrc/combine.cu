@@ -15,9 +15,10 @@
 //
 // One warp handles one (token, 512-channel segment) item: every lane issues
 // all k row loads of its 2 x 16 bytes before the first fma (k*2 independent
-// 16-byte streaming loads in flight per lane), then reduces in registers and
-// stores 2 x 16 bytes of bf16.  Rows are read whole and in order, so every
-// warp load instruction moves 512 contiguous bytes.
+// 16-byte streaming loads in flight per lane, marked evict-first in L2: each
+// row is read once, and the dispatch's output may still be in L2), then
+// reduces in registers and stores 2 x 16 bytes of bf16.  Rows are read whole
+// and in order, so every warp load instruction moves 512 contiguous bytes.
 
 #include "ep_common.cuh"
 
@@ -43,6 +44,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineParams p)
   // the kernel that wrote combine_idx (the dispatch) has finished
   pdl_wait();
   const int lane = threadIdx.x & 31;
+  const uint64_t pol = l2_policy_evict_first();   // every expert-output row is read once
   const int64_t warp0 = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCombineThreads) >> 5;
   const int64_t row_bytes = (int64_t)p.H * 2;
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineParams p)
 #pragma unroll
       for (int j = 0; j < kK; ++j) {
         if (j < p.k && f[j] >= 0 && ch < p.H)
-          v[u][j] = ld_stream_v4(p.y + (int64_t)f[j] * row_bytes + (int64_t)ch * 2);
+          v[u][j] = ld_stream_v4(p.y + (int64_t)f[j] * row_bytes + (int64_t)ch * 2, pol);
         else
           v[u][j] = make_uint4(0, 0, 0, 0);
       }

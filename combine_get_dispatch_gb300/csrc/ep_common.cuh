@@ -124,12 +124,21 @@ __device__ __forceinline__ void named_barrier_sync(int id, int n) {
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// 16-byte read-only streaming load (data not reused by this SM).
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+// L2 policy for data read exactly once: its lines are the first to go, so a
+// stream of them does not push other lines (and their write-backs) out.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte read-only streaming load (data not reused by this SM), with an
+// L2 cache policy (l2_policy_evict_first for read-once data).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p, uint64_t pol) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return v;
 }
 
