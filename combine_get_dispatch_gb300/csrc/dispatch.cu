@@ -459,10 +459,11 @@ __global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterPar
 //      global exclusive count of its expert (§1.2, §3.2) -- and writes
 //      combine_idx and src_info for the tokens whose first piece it holds
 //      (the CTA holding the last token writes recv_count);
-//   3. only now bulk-loads its x pieces (a read issued while ~30 MB of bulk
-//      loads are queued waits behind them, and steps 0-2 are a chain of such
-//      reads); as each lands: bf16 -- issue its k bulk stores; FP8 --
-//      quantise it in place, staging the token's block scales row-major;
+//   3. only now bulk-loads the rest of its x pieces -- two per warp went out
+//      with the ids -- (a read issued while ~30 MB of bulk loads are queued
+//      waits behind them, and steps 0-2 are a chain of such reads); as each
+//      lands: bf16 -- issue its k bulk stores; FP8 -- quantise it in place,
+//      staging the token's block scales row-major;
 //   4. arrives at a grid barrier (workspace counter).  FP8: warps 0..11 issue
 //      the k bulk stores of every unit while warps 12..15 wait for the
 //      barrier and write the per-expert outputs of the experts
@@ -478,6 +479,7 @@ constexpr int kFusedWarps = 16;
 constexpr int kStoreWarps = 12;          // FP8: warps issuing the bulk stores; the rest write the scales
 constexpr int kFusedMaxPerWarp = 8;      // units per warp
 constexpr int kFusedPiece = 1024;        // channels per unit
+constexpr int kEarlyUnits = 2;           // units per warp loaded at kernel start
 constexpr int kRankWarps = 8;            // warps that rank a CTA's own slots
 constexpr int kRankIdsPerLane = 4;
 constexpr int kMaxOwnIds = kRankWarps * kWarp * kRankIdsPerLane;
@@ -692,6 +694,22 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
     }
   };
   load_scan(scan_lo);
+  // the first kEarlyUnits pieces of every warp go out right behind the ids
+  // (a small queue of loads: the id chain barely notices it), so stores can
+  // start the moment the ranks are known
+  auto load_unit = [&](int32_t m) {
+    int32_t g;
+    int pc;
+    unit_of(m, &g, &pc);
+    const uint32_t bytes = (uint32_t)min(p.Hp, p.H - pc * p.Hp) * 2u;
+    mbar_arrive_expect_tx(&bars[m], bytes);
+    tma_load_1d(unit_slot(m), p.x + (int64_t)g * p.H * 2 + (int64_t)pc * p.Hp * 2, bytes, &bars[m]);
+  };
+  if (nm > 0 && lane == 0) {
+    for (int32_t m = 0; m < nm; ++m) mbar_init(&bars[m], 1);
+    fence_barrier_init();
+    for (int32_t m = 0; m < min(nm, kEarlyUnits); ++m) load_unit(m);
+  }
   for (int i = tid; i < (2 + kRankWarps) * p.E; i += kThreads) s_P[i] = 0;   // s_P, s_cnt, s_H
   if (tid == 0) {
     s_epoch = ld_relaxed_u32(&p.ctl[kCtlEpoch]);
@@ -827,20 +845,11 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
       }
     }
   }
-  // every source piece of this CTA in flight, only now: a read issued while
-  // ~30 MB of bulk loads are queued waits behind them, and the steps above
-  // are one chain of such reads
+  // the rest of this CTA's source pieces in flight, only now: a read issued
+  // while ~30 MB of bulk loads are queued waits behind them, and the steps
+  // above are one chain of such reads
   if (nm > 0 && lane == 0) {
-    for (int32_t m = 0; m < nm; ++m) mbar_init(&bars[m], 1);
-    fence_barrier_init();
-    for (int32_t m = 0; m < nm; ++m) {
-      int32_t g;
-      int pc;
-      unit_of(m, &g, &pc);
-      const uint32_t bytes = (uint32_t)min(p.Hp, p.H - pc * p.Hp) * 2u;
-      mbar_arrive_expect_tx(&bars[m], bytes);
-      tma_load_1d(unit_slot(m), p.x + (int64_t)g * p.H * 2 + (int64_t)pc * p.Hp * 2, bytes, &bars[m]);
-    }
+    for (int32_t m = min(nm, kEarlyUnits); m < nm; ++m) load_unit(m);
   }
   __syncthreads();
 

@@ -58,8 +58,16 @@ def test_layout_edge_shapes(R, T_r, k, E):
     rng = np.random.default_rng(R * 1000 + T_r)
     idx = rng.integers(-1, E, size=(R, T_r, k)).astype(np.int64)
     lay = gpu_layout(torch.from_numpy(idx).cuda(), E)
-    _compare_layout(idx, E, lay)
+    ref = _compare_layout(idx, E, lay)
     assert ep.ep_read_status(lay["status"]) == ep.EP_OK
+    # notify on the same counts: column walks over R source ranks in
+    # batches (R = 1 .. 64 here, ragged against the batch of 16)
+    for A in (1, 8):
+        nt = gpu_notify(lay, E, A)
+        nref = oracle.notify(ref["num_tokens_per_rank"], ref["num_tokens_per_expert"], R, E, A)
+        for key in NOTIFY_KEYS:
+            assert np.array_equal(np_(nt[key]), nref[key]), key
+        assert ep.ep_read_status(nt["status"]) == ep.EP_OK
 
 
 def test_layout_all_tokens_to_one_expert():
