@@ -2,6 +2,8 @@
 
 #include <atomic>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "ep_common.cuh"
 
@@ -34,6 +36,24 @@ void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_r
 int check_launch() {
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+int ensure_max_smem(const void* func, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({func, dev})) return EP_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
+  done.insert({func, dev});
+  return EP_OK;
 }
 
 }  // namespace ep_host

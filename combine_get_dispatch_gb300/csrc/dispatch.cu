@@ -1007,14 +1007,9 @@ static bool plan_fused(FusedParams& p, int grid) {
 
 template <int kMode>
 static int launch_fused_t(const FusedParams& p, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(k_ll_fused<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kFusedSmemCap) != cudaSuccess) {
-      cudaGetLastError();
-      return EP_ERR_CUDA;
-    }
-    attr_set = true;
+  {
+    const int rc = ep_host::ensure_max_smem(reinterpret_cast<const void*>(k_ll_fused<kMode>), (int)kFusedSmemCap);
+    if (rc != EP_OK) return rc;
   }
   k_ll_fused<kMode><<<grid, kFusedWarps * kWarp, fused_smem(p), stream>>>(p);
   ep_host::count_launch();
@@ -1233,14 +1228,9 @@ static int launch_scatter_t(ScatterParams p, cudaStream_t stream, bool pdl) {
   p.n_units = p.T * p.P;
   if (p.n_units > INT32_MAX) return EP_ERR_INVALID_ARG;
   const size_t smem = (size_t)p.warps_per_cta * p.warp_smem;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(k_scatter<kMode, kLL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kScatterSmemBudget + 1024) != cudaSuccess) {
-      cudaGetLastError();
-      return EP_ERR_CUDA;
-    }
-    attr_set = true;
+  {
+    const int rc = ep_host::ensure_max_smem(reinterpret_cast<const void*>(k_scatter<kMode, kLL>), (int)kScatterSmemBudget + 1024);
+    if (rc != EP_OK) return rc;
   }
   const int64_t work = std::max<int64_t>(p.n_units, p.n_pad_items);
   const int64_t want = (work + p.warps_per_cta - 1) / p.warps_per_cta;

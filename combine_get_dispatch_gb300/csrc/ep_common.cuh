@@ -267,5 +267,8 @@ namespace ep_host {
 int num_sms();
 void count_launch(int n = 1);
 int check_launch();   // EP_OK or EP_ERR_CUDA after a launch
+// Opt a kernel into `bytes` of dynamic shared memory on the current device
+// (once per kernel and device: the attribute is per device).
+int ensure_max_smem(const void* func, int bytes);
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace ep_host

@@ -340,14 +340,9 @@ static int launch_layout_t(LayoutParams p, void* ws, cudaStream_t stream) {
   auto smem_bytes = [](int E, int V) {
     return sizeof(int32_t) * ((size_t)kThreads * kIdsPerLane + (size_t)(kThreads / kWarp) * E + 2 * (size_t)V);
   };
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(k_layout<kLL, kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes(kMaxE, kMaxE + kMaxR)) != cudaSuccess) {
-      cudaGetLastError();
-      return EP_ERR_CUDA;
-    }
-    attr_set = true;
+  {
+    const int rc = ep_host::ensure_max_smem(reinterpret_cast<const void*>(k_layout<kLL, kThreads>), (int)smem_bytes(kMaxE, kMaxE + kMaxR));
+    if (rc != EP_OK) return rc;
   }
   k_layout<kLL, kThreads><<<p.num_chunks, kThreads, smem_bytes(p.E, p.V), stream>>>(p);
   ep_host::count_launch();
