@@ -461,22 +461,24 @@ __global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterPar
 //      (the CTA holding the last token writes recv_count);
 //   3. only now bulk-loads the rest of its x pieces -- two per warp went out
 //      with the ids -- (a read issued while ~30 MB of bulk loads are queued
-//      waits behind them, and steps 0-2 are a chain of such reads); as each
-//      lands: bf16 -- issue its k bulk stores; FP8 -- quantise it in place,
-//      staging the token's block scales row-major;
-//   4. arrives at a grid barrier (workspace counter).  FP8: warps 0..11 issue
-//      the k bulk stores of every unit while warps 12..15 wait for the
-//      barrier and write the per-expert outputs of the experts
-//      e = cta + n * grid as the stores drain: layout_range from the sources
-//      of their rows (sorted by token, so each rank is one run) and the
-//      column-major scales, coalesced along rows.  bf16: every warp waits
-//      and writes layout_range.
+//      waits behind them, and steps 0-2 are a chain of such reads).
+//      bf16: as each lands, its k bulk stores go out.  FP8: warps 0..11 own
+//      the units, quantise each in place as it lands (staging the token's
+//      block scales row-major) and mark it on a per-unit mbarrier; warps
+//      12..15 issue each unit's k bulk stores the moment it is marked, so
+//      the store stream starts with the first quantised piece;
+//   4. the unit warps (bf16: all warps) arrive at a grid barrier (workspace
+//      counter), wait for every CTA, and write the per-expert outputs of
+//      the experts e = cta + n * grid while the stores drain: layout_range
+//      from the sources of their rows (sorted by token, so each rank is one
+//      run) and (FP8) the column-major scales, coalesced along rows.
 // All CTAs are resident at once (one per SM, grid = SM count), so the waits
 // on other CTAs (chunk words, the barrier) end; every wait is bounded anyway
 // and gives up with EP_ERR_TIMEOUT.
 
 constexpr int kFusedWarps = 16;
-constexpr int kStoreWarps = 12;          // FP8: warps issuing the bulk stores; the rest write the scales
+constexpr int kQuantWarps = 12;          // FP8: warps owning (loading, quantising) units; the
+                                         // other 4 issue the bulk stores as units are quantised
 constexpr int kFusedMaxPerWarp = 8;      // units per warp
 constexpr int kFusedPiece = 1024;        // channels per unit
 constexpr int kEarlyUnits = 2;           // units per warp loaded at kernel start
@@ -484,7 +486,7 @@ constexpr int kRankWarps = 8;            // warps that rank a CTA's own slots
 constexpr int kRankIdsPerLane = 4;
 constexpr int kMaxOwnIds = kRankWarps * kWarp * kRankIdsPerLane;
 constexpr int kFusedChunkIds = 1024;     // ids per published histogram
-constexpr int kFusedBarBytes = kFusedWarps * kFusedMaxPerWarp * 8;
+constexpr int kFusedBarBytes = 2 * kFusedWarps * kFusedMaxPerWarp * 8;   // load + quantised barriers
 constexpr size_t kFusedSmemCap = 225 * 1024;
 constexpr int kCtlArrive = 8;            // workspace control words of this kernel
 constexpr int kCtlExit = 9;
@@ -528,6 +530,7 @@ struct FusedParams {
   int own_cap;               // own-id capacity (multiple of 32)
   int nA;                    // experts per CTA (ceil(E / grid))
   int nbits;
+  bool fp8;                  // FP8 modes: units owned by kQuantWarps warps
 };
 
 // Per-expert outputs of the fused path for this CTA's experts e = cta + a * grid
@@ -644,18 +647,24 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   const int32_t U = p.n_units;
   const int32_t u0 = (int32_t)((int64_t)U * cta / grid);
   const int32_t u1 = (int32_t)((int64_t)U * (cta + 1) / grid);
-  const int32_t nm = warp < u1 - u0 ? (u1 - u0 - warp + kFusedWarps - 1) / kFusedWarps : 0;
+  // FP8: warps 0..kQuantWarps-1 own (load, quantise) the units, the rest
+  // issue their bulk stores; bf16: every warp owns units and stores them
+  constexpr int kOwnWarps = kFp8 ? kQuantWarps : kFusedWarps;
+  const int32_t nm = (warp < kOwnWarps && warp < u1 - u0)
+                         ? (u1 - u0 - warp + kOwnWarps - 1) / kOwnWarps : 0;
   uint8_t* slots = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.slot_area) + warp * kFusedMaxPerWarp;
+  // FP8: one "quantised" barrier per unit of the CTA (slot index q = u - u0)
+  uint64_t* qbars = reinterpret_cast<uint64_t*>(smem + p.slot_area) + kFusedWarps * kFusedMaxPerWarp;
   int32_t* s_P = reinterpret_cast<int32_t*>(smem + p.slot_area + kFusedBarBytes);   // [E]
   int32_t* s_cnt = s_P + p.E;                    // [kRankWarps][E]
   int32_t* s_H = s_cnt + kRankWarps * p.E;       // [E] histogram of chunk `cta`
   int32_t* s_own = s_H + p.E;                    // [own_cap] own ids
   int32_t* s_f = s_own + p.own_cap;              // [own_cap] their packed rows
   int32_t* s_lo = s_f + p.own_cap;               // [nA][R + 1] first row of every rank
-  auto unit_slot = [&](int32_t m) { return slots + (size_t)(warp + m * kFusedWarps) * p.slot_bytes; };
+  auto unit_slot = [&](int32_t m) { return slots + (size_t)(warp + m * kOwnWarps) * p.slot_bytes; };
   auto unit_of = [&](int32_t m, int32_t* g, int* pc) {
-    const int32_t u = u0 + warp + m * kFusedWarps;
+    const int32_t u = u0 + warp + m * kOwnWarps;
     *g = u / p.P;
     *pc = u - *g * p.P;
   };
@@ -705,6 +714,10 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
     mbar_arrive_expect_tx(&bars[m], bytes);
     tma_load_1d(unit_slot(m), p.x + (int64_t)g * p.H * 2 + (int64_t)pc * p.Hp * 2, bytes, &bars[m]);
   };
+  if (kFp8 && tid == kThreads - 1) {
+    for (int32_t q = 0; q < u1 - u0; ++q) mbar_init(&qbars[q], 1);
+    fence_barrier_init();
+  }
   if (nm > 0 && lane == 0) {
     for (int32_t m = 0; m < nm; ++m) mbar_init(&bars[m], 1);
     fence_barrier_init();
@@ -853,108 +866,121 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   }
   __syncthreads();
 
-  // ---- 3. quantise (FP8) in place as the pieces land, staging each token's
-  //      scales row-major; bf16 units are stored as they land
+  // ---- 3. bf16: every warp stores its units as they land.  FP8: the unit
+  //      warps quantise their units in place as they land (staging each
+  //      token's scales row-major) and mark each one quantised; the store
+  //      warps issue each unit's k bulk stores as soon as it is marked
   const int64_t row_bytes = kFp8 ? (int64_t)p.H : (int64_t)p.H * 2;
-  for (int32_t m = 0; m < nm; ++m) {
-    const bool landed = mbar_wait_bounded(&bars[m], 0);
-    if (!__all_sync(0xffffffffu, landed)) {
-      set_status(p.status, EP_ERR_TIMEOUT);
-      s_units_ok = 0;
-      if (lane == 0)   // wait (bounded) for what is still in flight
-        for (int32_t r = m; r < nm; ++r) mbar_wait_bounded(&bars[r], 0);
-      break;
-    }
-    int32_t g;
-    int pc;
-    unit_of(m, &g, &pc);
-    const int hc = min(p.Hp, p.H - pc * p.Hp);
-    uint8_t* sl = unit_slot(m);
-    if (kFp8) {
-      uint8_t* srow = p.scale_rows + (int64_t)g * p.scale_row_bytes;
-      constexpr int kSegs = kFusedPiece / 512;
-      uint4 a[kSegs], b[kSegs];
-#pragma unroll
-      for (int sg = 0; sg < kSegs; ++sg) {
-        const int c0 = sg * 512 + lane * 16;
-        a[sg] = make_uint4(0, 0, 0, 0);
-        b[sg] = a[sg];
-        if (c0 < hc) {
-          a[sg] = ld_shared_v4(sl + (size_t)c0 * 2);
-          b[sg] = ld_shared_v4(sl + (size_t)c0 * 2 + 16);
-        }
-      }
-      __syncwarp();   // every lane has read its bf16 before any E4M3 lands on top
-#pragma unroll
-      for (int sg = 0; sg < kSegs; ++sg) {
-        const int c0 = sg * 512 + lane * 16;
-        float sf;
-        uint32_t su;
-        const uint4 qv = quantize16<kMode>(a[sg], b[sg], &sf, &su);
-        if (c0 < hc) {
-          st_shared_v4(sl + c0, qv);
-          if ((lane & 7) == 0) {
-            const int blk = (pc * p.Hp + c0) >> 7;
-            if (kEs == 4) reinterpret_cast<float*>(srow)[blk] = sf;
-            else srow[blk] = (uint8_t)su;
+  const int32_t n_own_units = u1 - u0;
+  if (!kFp8 || warp < kQuantWarps) {
+    for (int32_t m = 0; m < nm; ++m) {
+      const bool landed = mbar_wait_bounded(&bars[m], 0);
+      if (!__all_sync(0xffffffffu, landed)) {
+        set_status(p.status, EP_ERR_TIMEOUT);
+        s_units_ok = 0;
+        if (lane == 0) {   // wait (bounded) for what is still in flight; release the store warps
+          for (int32_t r = m; r < nm; ++r) {
+            mbar_wait_bounded(&bars[r], 0);
+            if (kFp8) mbar_arrive(&qbars[warp + r * kOwnWarps]);
           }
         }
+        break;
       }
-    } else if (lane < p.k) {
-      const int32_t f = s_f[(g - ga) * p.k + lane];
-      if (f >= 0)
-        tma_store_1d(p.recv_x + f * row_bytes + (int64_t)pc * p.Hp * 2, sl, (uint32_t)hc * 2u);
-      tma_commit();
-    }
-  }
-  if (kFp8) fence_proxy_async_smem();   // the E4M3 pieces are read by bulk stores
-  __syncthreads();   // this CTA's src_info and staged scales are written
-
-  // ---- 4. grid barrier, then the per-expert outputs: layout_range and (FP8)
-  //      the column-major scales of this CTA's experts e = cta + a * grid.
-  //      FP8: warps 0..kStoreWarps-1 issue the bulk stores of every unit
-  //      meanwhile, so the scale pass runs while the stores drain.
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&p.ctl[kCtlArrive], 1u) >= (uint32_t)grid) {   // workspace not cleaned
-      set_status(p.status, EP_ERR_STATE);
-      s_ok = 0;
-    }
-  }
-  // s_ok is final from here on: every thread that branches on it below (some
-  // of them before a named barrier) reads the same value
-  __syncthreads();
-  const int32_t n_own_units = u1 - u0;
-  if (kFp8 && warp < kStoreWarps) {
-    if (s_units_ok) {
-      for (int32_t q = warp; q < n_own_units; q += kStoreWarps) {
-        const int32_t u = u0 + q;
-        const int32_t g = u / p.P;
-        const int pc = u - g * p.P;
-        const int hc = min(p.Hp, p.H - pc * p.Hp);
-        if (lane < p.k) {
-          const int32_t f = s_f[(g - ga) * p.k + lane];
-          if (f >= 0)
-            tma_store_1d(p.recv_x + f * row_bytes + (int64_t)pc * p.Hp, slots + (size_t)q * p.slot_bytes,
-                         (uint32_t)hc);
-          tma_commit();
+      int32_t g;
+      int pc;
+      unit_of(m, &g, &pc);
+      const int hc = min(p.Hp, p.H - pc * p.Hp);
+      uint8_t* sl = unit_slot(m);
+      if (kFp8) {
+        uint8_t* srow = p.scale_rows + (int64_t)g * p.scale_row_bytes;
+        constexpr int kSegs = kFusedPiece / 512;
+        uint4 a[kSegs], b[kSegs];
+#pragma unroll
+        for (int sg = 0; sg < kSegs; ++sg) {
+          const int c0 = sg * 512 + lane * 16;
+          a[sg] = make_uint4(0, 0, 0, 0);
+          b[sg] = a[sg];
+          if (c0 < hc) {
+            a[sg] = ld_shared_v4(sl + (size_t)c0 * 2);
+            b[sg] = ld_shared_v4(sl + (size_t)c0 * 2 + 16);
+          }
         }
+        __syncwarp();   // every lane has read its bf16 before any E4M3 lands on top
+#pragma unroll
+        for (int sg = 0; sg < kSegs; ++sg) {
+          const int c0 = sg * 512 + lane * 16;
+          float sf;
+          uint32_t su;
+          const uint4 qv = quantize16<kMode>(a[sg], b[sg], &sf, &su);
+          if (c0 < hc) {
+            st_shared_v4(sl + c0, qv);
+            if ((lane & 7) == 0) {
+              const int blk = (pc * p.Hp + c0) >> 7;
+              if (kEs == 4) reinterpret_cast<float*>(srow)[blk] = sf;
+              else srow[blk] = (uint8_t)su;
+            }
+          }
+        }
+        fence_proxy_async_smem();   // the E4M3 piece is read by bulk stores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qbars[warp + m * kOwnWarps]);
+      } else if (lane < p.k) {
+        const int32_t f = s_f[(g - ga) * p.k + lane];
+        if (f >= 0)
+          tma_store_1d(p.recv_x + f * row_bytes + (int64_t)pc * p.Hp * 2, sl, (uint32_t)hc * 2u);
+        tma_commit();
       }
     }
   } else {
-    const int t0 = kFp8 ? tid - kStoreWarps * kWarp : tid;
-    const int nt = kFp8 ? kThreads - kStoreWarps * kWarp : kThreads;
+    // FP8 store warps: units in slot order, each once it is quantised
+    for (int32_t q = warp - kQuantWarps; q < n_own_units; q += kFusedWarps - kQuantWarps) {
+      const bool ready = mbar_wait_bounded(&qbars[q], 0);
+      if (!__all_sync(0xffffffffu, ready)) {
+        set_status(p.status, EP_ERR_TIMEOUT);
+        break;
+      }
+      if (!s_units_ok) continue;
+      const int32_t u = u0 + q;
+      const int32_t g = u / p.P;
+      const int pc = u - g * p.P;
+      const int hc = min(p.Hp, p.H - pc * p.Hp);
+      if (lane < p.k) {
+        const int32_t f = s_f[(g - ga) * p.k + lane];
+        if (f >= 0)
+          tma_store_1d(p.recv_x + f * row_bytes + (int64_t)pc * p.Hp,
+                       slots + (size_t)q * p.slot_bytes, (uint32_t)hc);
+        tma_commit();
+      }
+    }
+  }
+
+  // ---- 4. grid barrier, then the per-expert outputs of this CTA's experts
+  //      e = cta + a * grid: layout_range and (FP8) the column-major scales.
+  //      FP8: the unit warps do it while the store warps keep issuing;
+  //      bf16: every warp, once its stores are issued.
+  if (!kFp8 || warp < kQuantWarps) {
+    constexpr int kGroup = kFp8 ? kQuantWarps * kWarp : kThreads;
     auto sync = [&]() {
-      if (kFp8) named_barrier_sync(1, kThreads - kStoreWarps * kWarp);
+      if (kFp8) named_barrier_sync(1, kGroup);
       else __syncthreads();
     };
-    if (t0 == 0) {   // the group's leader alone writes s_passed; the group reads it after sync()
-      s_passed = wait_count(&p.ctl[kCtlArrive], (uint32_t)grid) ? 1 : 0;
-      if (!s_passed) set_status(p.status, EP_ERR_TIMEOUT);
+    sync();   // the group's staged scales (and src_info, written before) are out
+    if (tid == 0) {   // the group leader alone writes s_passed
       __threadfence();
+      int passed = 1;
+      if (atomicAdd(&p.ctl[kCtlArrive], 1u) >= (uint32_t)grid) {   // workspace not cleaned
+        set_status(p.status, EP_ERR_STATE);
+        passed = 0;
+      }
+      if (passed && !wait_count(&p.ctl[kCtlArrive], (uint32_t)grid)) {
+        set_status(p.status, EP_ERR_TIMEOUT);
+        passed = 0;
+      }
+      __threadfence();
+      s_passed = passed;
     }
-    sync();
-    if (s_ok && s_passed) fused_expert_outputs<kFp8, kEs>(p, cta, grid, t0, nt, s_P, s_lo, sync);
+    sync();   // s_ok (settled before step 3) and s_passed are read by the whole group
+    if (s_ok && s_passed) fused_expert_outputs<kFp8, kEs>(p, cta, grid, tid, kGroup, s_P, s_lo, sync);
   }
   __syncthreads();
   pdl_launch_dependents();   // a dependent combine may take its place as this drains
@@ -989,7 +1015,8 @@ static bool plan_fused(FusedParams& p, int grid) {
   p.P = (p.H + hp - 1) / hp;
   const int64_t units = (int64_t)p.T * p.P;
   const int64_t per_cta = (units + grid - 1) / grid;
-  if (per_cta > (int64_t)kFusedWarps * kFusedMaxPerWarp) return false;
+  // units per CTA: at most kFusedMaxPerWarp per unit-owning warp
+  if (per_cta > (int64_t)(p.fp8 ? kQuantWarps : kFusedWarps) * kFusedMaxPerWarp) return false;
   p.n_units = (int32_t)units;
   p.slot_bytes = round128((uint32_t)hp * 2u);
   p.slot_area = (uint32_t)(per_cta * p.slot_bytes);
@@ -1410,6 +1437,7 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
     (void)chunks;
     fp.chunk_hist = reinterpret_cast<uint64_t*>(fr);
     fp.status = status;
+    fp.fp8 = fp8;
     if (ep::plan_fused(fp, grid))
       return ep::launch_fused(fp, fp8_mode, grid, s);
   }
