@@ -459,8 +459,8 @@ __global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterPar
 //      global exclusive count of its expert (§1.2, §3.2) -- and writes
 //      combine_idx and src_info for the tokens whose first piece it holds
 //      (the CTA holding the last token writes recv_count);
-//   3. only now bulk-loads the rest of its x pieces -- two per warp went out
-//      with the ids -- (a read issued while ~30 MB of bulk loads are queued
+//   3. only now bulk-loads the rest of its x pieces -- one per unit warp
+//      went out with the ids -- (a read issued while ~30 MB of bulk loads are queued
 //      waits behind them, and steps 0-2 are a chain of such reads).
 //      bf16: as each lands, its k bulk stores go out.  FP8: warps 0..11 own
 //      the units, quantise each in place as it lands (staging the token's
@@ -481,7 +481,7 @@ constexpr int kQuantWarps = 12;          // FP8: warps owning (loading, quantisi
                                          // other 4 issue the bulk stores as units are quantised
 constexpr int kFusedMaxPerWarp = 8;      // units per warp
 constexpr int kFusedPiece = 1024;        // channels per unit
-constexpr int kEarlyUnits = 2;           // units per warp loaded at kernel start
+constexpr int kEarlyUnits = 1;           // units per warp loaded at kernel start
 constexpr int kRankWarps = 8;            // warps that rank a CTA's own slots
 constexpr int kRankIdsPerLane = 4;
 constexpr int kMaxOwnIds = kRankWarps * kWarp * kRankIdsPerLane;
