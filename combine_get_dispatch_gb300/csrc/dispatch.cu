@@ -712,7 +712,8 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
     unit_of(m, &g, &pc);
     const uint32_t bytes = (uint32_t)min(p.Hp, p.H - pc * p.Hp) * 2u;
     mbar_arrive_expect_tx(&bars[m], bytes);
-    tma_load_1d(unit_slot(m), p.x + (int64_t)g * p.H * 2 + (int64_t)pc * p.Hp * 2, bytes, &bars[m]);
+    tma_load_1d_hint(unit_slot(m), p.x + (int64_t)g * p.H * 2 + (int64_t)pc * p.Hp * 2, bytes, &bars[m],
+                     l2_policy_evict_first());   // every token is read once
   };
   if (kFp8 && tid == kThreads - 1) {
     for (int32_t q = 0; q < u1 - u0; ++q) mbar_init(&qbars[q], 1);
