@@ -686,6 +686,7 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   // ---- 0. the ids: they are on the critical path, so they go out before any
   //      bulk load of x (which would queue them behind ~30 MB of reads)
   constexpr int kScanPairs = 2;                     // 16-byte id loads per thread per pass
+  static_assert(2 * kThreads >= kFusedChunkIds, "one 16-byte load per thread covers a chunk");
   longlong2 vc = make_longlong2(-1, -1);
   longlong2 vs[kScanPairs];
   {
