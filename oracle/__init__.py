@@ -88,6 +88,12 @@ def _declare(L: ctypes.CDLL) -> None:
     L.ep_oracle_ll_dispatch.restype = _I
     L.ep_oracle_combine.argtypes = [_P, _P, _P, _I64, _I64, _I, _I, _P]
     L.ep_oracle_combine.restype = _I
+    L.ep_oracle_rank_dispatch.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I64,
+                                          _P, _P, _P, _P, _P, _P]
+    L.ep_oracle_rank_dispatch.restype = _I
+    L.ep_oracle_rank_combine.argtypes = [_P, _P, _I64, _I64, _I, _I, _P]
+    L.ep_oracle_rank_combine.restype = _I
+    L.ep_oracle_combine.restype = _I
 
 
 def _ptr(a: np.ndarray | None) -> int | None:
@@ -252,4 +258,36 @@ def combine(y: np.ndarray, topk_weights: np.ndarray, combine_idx: np.ndarray, H:
     out = np.empty(cidx.shape[:-1] + (H,), np.uint16)
     rc = lib().ep_oracle_combine(_ptr(y), _ptr(w), _ptr(cidx), y.shape[0], n_tokens, H, k,
                                  _ptr(out))
+    return dict(rc=rc, out=out)
+
+
+def rank_dispatch(x: np.ndarray, topk_idx: np.ndarray, topk_weights: np.ndarray, E: int,
+                  fp8_mode: int, cap_rows: int, fill: int = 0):
+    """Once-per-rank receive layout (V1 normal mode).  x [R, T_r, H] bf16
+    bits; rows holding no token keep `fill` (recv_topk_* keep -1 / 0)."""
+    x = _c(x, np.uint16)
+    idx = _c(topk_idx, np.int64)
+    w = _c(topk_weights, np.float32)
+    R, T_r, H = x.shape
+    k = idx.shape[2]
+    recv, scales = _recv_buffers(R, cap_rows, H, fp8_mode, fill)
+    src = np.zeros((R, cap_rows), np.int32)
+    rtk = np.full((R, cap_rows, k), -1, np.int64)
+    rtw = np.zeros((R, cap_rows, k), np.float32)
+    cidx = np.zeros((R, T_r, k), np.int32)
+    rc = lib().ep_oracle_rank_dispatch(_ptr(x), _ptr(idx), _ptr(w), R, T_r, H, E, k, fp8_mode,
+                                       cap_rows, _ptr(recv), _ptr(scales), _ptr(src), _ptr(rtk),
+                                       _ptr(rtw), _ptr(cidx))
+    return dict(rc=rc, recv_x=recv, recv_scales=scales, recv_src_idx=src, recv_topk_idx=rtk,
+                recv_topk_weights=rtw, combine_idx=cidx)
+
+
+def rank_combine(y: np.ndarray, combine_idx: np.ndarray, H: int):
+    """Sum over destination ranks of y rows (bf16 bits viewed [n_rows, H])."""
+    y = _c(y, np.uint16).reshape(-1, H)
+    cidx = _c(combine_idx, np.int32)
+    k = cidx.shape[-1]
+    n_tokens = cidx.size // k
+    out = np.empty(cidx.shape[:-1] + (H,), np.uint16)
+    rc = lib().ep_oracle_rank_combine(_ptr(y), _ptr(cidx), y.shape[0], n_tokens, H, k, _ptr(out))
     return dict(rc=rc, out=out)

@@ -20,7 +20,11 @@
  *   §3.2 low-latency routing (dst_rank = expert / num_local_experts),
  *   §4.3 EPHandle (psum_num_recv_tokens_per_expert = aligned prefix sum =
  *        segment start of each expert in the receive buffer; combine is
- *        dispatch walked backwards).
+ *        dispatch walked backwards);
+ *   V1's once-per-rank receive layout (§2.1, §2.3): a token goes once to
+ *        every rank holding one of its experts, at rank_prefix_matrix[i-1][r]
+ *        plus its position among source rank i's tokens for r, and the
+ *        combine sums the rows the ranks return.
  * Number formats: OCP 8-bit floating point specification (E4M3: bias 7,
  * max 448, no infinities, NaN = S.1111.111) and the bfloat16 format (top 16
  * bits of IEEE-754 binary32), both rounded to nearest, ties to even.
@@ -439,6 +443,135 @@ int ep_oracle_combine(const uint16_t* y, const float* topk_weights, const int32_
         int32_t f = combine_idx[t * k + j];
         if (f < 0) continue;
         acc = fmaf(topk_weights[t * k + j], ep_oracle_bf16_to_f32(y[(int64_t)f * H + h]), acc);
+      }
+      out[t * H + h] = ep_oracle_f32_to_bf16(acc);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Once-per-rank receive layout ([06_deepep §2.1, §2.3]: V1 normal mode) */
+/* ------------------------------------------------------------------ */
+
+/* Token t of source rank i goes ONCE to every rank r that holds one of its
+ * experts (is_token_in_rank[i][t][r]).  Rank r's buffer [cap_rows, H] holds
+ * source rank i's tokens in rows [rpm[i-1][r], rpm[i][r]) -- rpm the
+ * rank_prefix_matrix, inclusive over source ranks, rpm[-1] = 0 -- in token
+ * order:
+ *     row(i, t, r) = rpm[i-1][r] + #{ t' < t : is_token_in_rank[i][t'][r] }.
+ *   recv_x, recv_scales  as in dispatch, one row per (token, rank)
+ *   recv_src_idx     [R, cap_rows]    i*T_r + t, -1 where no token sits
+ *   recv_topk_idx    [R, cap_rows, k] per slot j of the row's token: its
+ *                    expert's local index e - r*E_l when that expert is on
+ *                    r, else -1 (rows holding no token are left untouched)
+ *   recv_topk_weights[R, cap_rows, k] the slot's weight when its expert is
+ *                    on r, else 0
+ *   combine_idx      [R, T_r, k]     r*cap_rows + row(i, t, r) at the token's
+ *                    FIRST slot whose expert is on r, -1 at every other slot
+ * rpm is computed here from the definition (count, then prefix), not taken
+ * from the caller.  A row at or past cap_rows is not written (its slot gets
+ * -1) and the call returns ORACLE_ERR_CAPACITY. */
+int ep_oracle_rank_dispatch(const uint16_t* x, const int64_t* topk_idx, const float* topk_weights,
+                            int R, int T_r, int H, int E, int k, int fp8_mode, int64_t cap_rows,
+                            void* recv_x, void* recv_scales, int32_t* recv_src_idx,
+                            int64_t* recv_topk_idx, float* recv_topk_weights,
+                            int32_t* combine_idx) {
+  if (R <= 0 || E % R != 0 || (fp8_mode != FP8_NONE && H % BLOCK_CHANNELS != 0))
+    return ORACLE_ERR_INVALID_ARG;
+  int E_l = E / R;
+  int nb = H / BLOCK_CHANNELS;
+  int rc = ORACLE_OK;
+  for (int64_t p = 0; p < (int64_t)R * T_r * k; ++p)
+    if (topk_idx[p] < -1 || topk_idx[p] >= E) return ORACLE_ERR_INVALID_ARG;
+  /* tokens of source rank i that go to rank r, and the inclusive prefix */
+  int64_t* cnt = (int64_t*)calloc((size_t)R * R, sizeof(int64_t));
+  for (int i = 0; i < R; ++i)
+    for (int t = 0; t < T_r; ++t)
+      for (int r = 0; r < R; ++r) {
+        int hit = 0;
+        for (int j = 0; j < k; ++j) {
+          int64_t e = topk_idx[((int64_t)i * T_r + t) * k + j];
+          if (e >= 0 && e / E_l == r) hit = 1;
+        }
+        cnt[(int64_t)i * R + r] += hit;
+      }
+  for (int64_t q = 0; q < (int64_t)R * cap_rows; ++q) recv_src_idx[q] = -1;
+  for (int r = 0; r < R; ++r) {
+    int64_t before = 0; /* rpm[i-1][r] */
+    for (int i = 0; i < R; ++i) {
+      int64_t pos = 0; /* tokens of rank i before t that go to r */
+      for (int t = 0; t < T_r; ++t) {
+        int64_t base = ((int64_t)i * T_r + t) * k;
+        int first = -1;
+        for (int j = 0; j < k; ++j) {
+          int64_t e = topk_idx[base + j];
+          if (e >= 0 && e / E_l == r) {
+            first = j;
+            break;
+          }
+        }
+        if (first < 0) continue;
+        int64_t row = before + pos;
+        pos += 1;
+        if (row >= cap_rows) {
+          combine_idx[base + first] = -1;
+          rc = ORACLE_ERR_CAPACITY;
+          continue;
+        }
+        int64_t flat = (int64_t)r * cap_rows + row;
+        put_row(x + ((int64_t)i * T_r + t) * H, H, fp8_mode, recv_x, flat, recv_scales,
+                (int64_t)r * nb * cap_rows + row, cap_rows);
+        recv_src_idx[flat] = i * T_r + t;
+        for (int j = 0; j < k; ++j) {
+          int64_t e = topk_idx[base + j];
+          int on_r = e >= 0 && e / E_l == r;
+          recv_topk_idx[flat * k + j] = on_r ? e - (int64_t)r * E_l : -1;
+          recv_topk_weights[flat * k + j] = on_r ? topk_weights[base + j] : 0.0f;
+        }
+        combine_idx[base + first] = (int32_t)flat;
+      }
+      before += cnt[(int64_t)i * R + r];
+    }
+  }
+  /* slots that are not a token's first slot on their rank */
+  for (int i = 0; i < R; ++i)
+    for (int t = 0; t < T_r; ++t) {
+      int64_t base = ((int64_t)i * T_r + t) * k;
+      for (int j = 0; j < k; ++j) {
+        int64_t e = topk_idx[base + j];
+        int first = e >= 0;
+        for (int jj = 0; jj < j && first; ++jj) {
+          int64_t ee = topk_idx[base + jj];
+          if (ee >= 0 && ee / E_l == e / E_l) first = 0;
+        }
+        if (!first) combine_idx[base + j] = -1;
+      }
+    }
+  free(cnt);
+  return rc;
+}
+
+/* Rank-level combine ([06_deepep §2.3]: dispatch walked backwards): every
+ * rank returns one row per token it received, already weighted by the
+ * experts that rank holds, and the rows are summed:
+ *     out[t][h] = bf16( sum in slot order over the slots j with
+ *                       combine_idx[t][j] >= 0 of y[combine_idx[t][j]][h] )
+ * in fp32 from +0 (one row per destination rank, at the token's first slot
+ * on that rank), rounded once. */
+int ep_oracle_rank_combine(const uint16_t* y, const int32_t* combine_idx, int64_t n_rows,
+                           int64_t n_tokens, int H, int k, uint16_t* out) {
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    for (int j = 0; j < k; ++j) {
+      int32_t f = combine_idx[t * k + j];
+      if (f < -1 || f >= n_rows) return ORACLE_ERR_INVALID_ARG;
+    }
+    for (int h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        int32_t f = combine_idx[t * k + j];
+        if (f < 0) continue;
+        acc = acc + ep_oracle_bf16_to_f32(y[(int64_t)f * H + h]);
       }
       out[t * H + h] = ep_oracle_f32_to_bf16(acc);
     }

@@ -151,3 +151,62 @@ def test_dispatch_full_size_sampled(name):
                 assert np.array_equal(got, q)
                 rr, rw = divmod(f, cap)
                 assert np.array_equal(np_(d["recv_scales"][rr, :, rw]), s)
+
+
+@pytest.mark.parametrize("fp8_mode", [0, 1])
+def test_fixed_shape_normal_path_replays_as_a_cuda_graph(fp8_mode):
+    """With num_worst_tokens the normal path needs no host round trip (the
+    receive shape is fixed), so layout -> notify -> dispatch -> combine can be
+    captured once into a CUDA graph; every replay with new routing and
+    activations copied into the captured buffers must match the oracle."""
+    w = synth.scaled(synth.WORKLOADS["skewed"], T_r=24, H=512, fp8_mode=fp8_mode,
+                     num_worst_tokens=32 * 24)
+    cap = w.cap_rows()
+    x_dev, _, idx_dev, _, wts_dev, _ = inputs(w)
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    status = status_word()
+    lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E)
+    nt = ep.alloc_notify(w.R, w.E)
+    d = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, fp8_mode, cap)
+    y = synth.expert_outputs_torch(w.R * cap, w.H, "cuda").view(w.R, cap, w.H)
+    out = torch.empty_like(x_dev)
+
+    def step():
+        ep.ep_get_dispatch_layout(idx_dev, w.E, lay["num_tokens_per_rank"],
+                                  lay["num_tokens_per_expert"], lay["is_token_in_rank"],
+                                  lay["slot_rank"], ws, status)
+        ep.ep_notify_dispatch(lay["num_tokens_per_rank"], lay["num_tokens_per_expert"], 1,
+                              w.num_worst_tokens, nt["rank_prefix_matrix"], nt["expert_prefix"],
+                              nt["num_recv_tokens_per_expert"], nt["psum"], None, 10000, status)
+        ep.ep_dispatch(x_dev, idx_dev, lay["slot_rank"], nt["expert_prefix"], nt["psum"], w.E,
+                       fp8_mode, cap, d["recv_x"], d["recv_scales"], d["recv_src_idx"],
+                       d["combine_idx"], ws, status)
+        ep.ep_combine(y, wts_dev, d["combine_idx"], cap, out, status)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    y_rows = np_(y).reshape(-1, w.H)
+    for seed in (7, 8):
+        _, x_host, _, idx, _, wts = inputs(w, seed=seed)
+        x_dev.copy_(torch.from_numpy(x_host.view(np.int16)).cuda().view(torch.bfloat16))
+        idx_dev.copy_(torch.from_numpy(idx).cuda())
+        wts_dev.copy_(torch.from_numpy(wts).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert ep.ep_read_status(status) == ep.EP_OK
+        _, _, ref, _ = oracle_normal(x_host, idx, w.E, 1, fp8_mode, cap_rows=cap,
+                                     num_worst_tokens=w.num_worst_tokens)
+        assert np.array_equal(np_(d["combine_idx"]), ref["combine_idx"])
+        assert np.array_equal(np_(d["recv_src_idx"]), ref["recv_src_idx"])
+        rows = np.nonzero(ref["recv_src_idx"].reshape(-1) >= 0)[0]
+        got_x = np_(d["recv_x"]).reshape(w.R * cap, -1)
+        assert np.array_equal(got_x[rows], ref["recv_x"].reshape(w.R * cap, -1)[rows])
+        want = oracle.combine(y_rows, wts, ref["combine_idx"], w.H)["out"]
+        assert np.array_equal(np_(out).reshape(want.shape), want)
