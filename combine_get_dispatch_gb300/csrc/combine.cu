@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineParams p)
     float my_w = 0.0f;
     if (lane < p.k) {
       my_f = p.cidx[g * p.k + lane];
-      my_w = p.w[g * p.k + lane];
+      my_w = p.w != nullptr ? p.w[g * p.k + lane] : 1.0f;   // no weights: a plain sum
       if (my_f < -1 || (int64_t)my_f >= p.n_rows) {
         if (s == 0) set_status(p.status, EP_ERR_INVALID_ARG);
         my_f = -1;
@@ -189,6 +189,27 @@ extern "C" int ep_ll_combine(const void* y, const float* topk_weights, const int
   p.w = topk_weights;
   p.cidx = combine_idx;
   p.n_rows = (int64_t)E * R * max_tokens_per_rank;
+  p.T = (int64_t)R * T_r;
+  p.H = H;
+  p.k = k;
+  p.out = static_cast<uint8_t*>(out);
+  p.status = status;
+  return ep::launch_combine(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ep_rank_combine(const void* y, const int32_t* combine_idx, int R, int T_r, int H,
+                               int k, int64_t cap_rows, void* out, int32_t* status, void* stream) {
+  // the rows are summed as they are: weight 1 (fma(1, y, acc) is acc + y, rounded once)
+  if (R <= 0 || R > ep::kMaxR || T_r < 0 || H <= 0 || H % 8 != 0 || k <= 0 || k > ep::kMaxK ||
+      cap_rows < 0)
+    return EP_ERR_INVALID_ARG;
+  if (T_r > 0 && (!y || !combine_idx || !out)) return EP_ERR_INVALID_ARG;
+  if (!ep_host::aligned16(y) || !ep_host::aligned16(out)) return EP_ERR_INVALID_ARG;
+  ep::CombineParams p{};
+  p.y = static_cast<const uint8_t*>(y);
+  p.w = nullptr;
+  p.cidx = combine_idx;
+  p.n_rows = (int64_t)R * cap_rows;
   p.T = (int64_t)R * T_r;
   p.H = H;
   p.k = k;

@@ -34,7 +34,8 @@ EP_FP8_E4M3_UE8M0 = 2
 EXPORTS = (
     "ep_workspace_size", "ep_get_dispatch_layout", "ep_notify_dispatch", "ep_dispatch",
     "ep_combine", "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_status",
-    "ep_host_wait_counters", "ep_launch_count", "ep_error_string",
+    "ep_host_wait_counters", "ep_launch_count", "ep_error_string", "ep_rank_ids",
+    "ep_rank_recv_topk", "ep_rank_combine",
 )
 
 
@@ -73,6 +74,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                  _SZ, _P, _P]
     L.ep_ll_combine.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]
     L.ep_clean_ll_buffer.argtypes = [_P, _I, _I, _P, _SZ, _P]
+    L.ep_rank_ids.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P]
+    L.ep_rank_recv_topk.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I64, _P, _P, _P, _P]
+    L.ep_rank_combine.argtypes = [_P, _P, _I, _I, _I, _I, _I64, _P, _P, _P]
     L.ep_read_status.argtypes = [_P, _P, _P]
     L.ep_host_wait_counters.argtypes = [_P, _I, _I]
     L.ep_launch_count.argtypes = []
@@ -81,7 +85,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.ep_error_string.restype = ctypes.c_char_p
     for name in ("ep_get_dispatch_layout", "ep_notify_dispatch", "ep_dispatch", "ep_combine",
                  "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_status",
-                 "ep_host_wait_counters"):
+                 "ep_host_wait_counters", "ep_rank_ids", "ep_rank_recv_topk", "ep_rank_combine"):
         getattr(L, name).restype = _I
     _lib = L
     return L
@@ -267,6 +271,43 @@ def ep_clean_ll_buffer(recv_count, num_ranks, num_experts, workspace, stream=Non
     rc = load().ep_clean_ll_buffer(_ptr(recv_count), num_ranks, num_experts, _ptr(workspace),
                                    0 if workspace is None else workspace.numel(), _stream(stream))
     _check(rc, "ep_clean_ll_buffer")
+
+
+def ep_rank_ids(topk_idx, num_experts, rank_ids, status=None, stream=None):
+    R, T_r, k = topk_idx.shape
+    _need(topk_idx, torch.int64, name="topk_idx")
+    _need(rank_ids, torch.int64, (R, T_r, k), "rank_ids")
+    _need(status, torch.int32, (1,), "status", optional=True)
+    rc = load().ep_rank_ids(_ptr(topk_idx), R, T_r, k, num_experts, _ptr(rank_ids), _ptr(status),
+                            _stream(stream))
+    _check(rc, "ep_rank_ids")
+
+
+def ep_rank_recv_topk(topk_idx, topk_weights, combine_idx, num_experts, cap_rows, recv_topk_idx,
+                      recv_topk_weights, status=None, stream=None):
+    R, T_r, k = topk_idx.shape
+    _need(topk_idx, torch.int64, name="topk_idx")
+    _need(topk_weights, torch.float32, (R, T_r, k), "topk_weights")
+    _need(combine_idx, torch.int32, (R, T_r, k), "combine_idx")
+    _need(recv_topk_idx, torch.int64, (R, cap_rows, k), "recv_topk_idx")
+    _need(recv_topk_weights, torch.float32, (R, cap_rows, k), "recv_topk_weights")
+    _need(status, torch.int32, (1,), "status", optional=True)
+    rc = load().ep_rank_recv_topk(_ptr(topk_idx), _ptr(topk_weights), _ptr(combine_idx), R, T_r,
+                                  k, num_experts, cap_rows, _ptr(recv_topk_idx),
+                                  _ptr(recv_topk_weights), _ptr(status), _stream(stream))
+    _check(rc, "ep_rank_recv_topk")
+
+
+def ep_rank_combine(y, combine_idx, cap_rows, out, status=None, stream=None):
+    R, T_r, k = combine_idx.shape
+    H = out.shape[2]
+    _need(y, torch.bfloat16, (R, cap_rows, H), "y")
+    _need(combine_idx, torch.int32, (R, T_r, k), "combine_idx")
+    _need(out, torch.bfloat16, (R, T_r, H), "out")
+    _need(status, torch.int32, (1,), "status", optional=True)
+    rc = load().ep_rank_combine(_ptr(y), _ptr(combine_idx), R, T_r, H, k, cap_rows, _ptr(out),
+                                _ptr(status), _stream(stream))
+    _check(rc, "ep_rank_combine")
 
 
 def ep_read_status(status, stream=None) -> int:

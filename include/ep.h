@@ -189,6 +189,56 @@ int ep_ll_combine(const void* y, const float* topk_weights, const int32_t* combi
                   int T_r, int H, int E, int k, int max_tokens_per_rank, void* out,
                   int32_t* status, void* stream);
 
+/* ---- once-per-rank receive layout (V1 normal mode, §2.1, §2.3) ----------
+ * A token goes ONCE to every rank holding one of its experts; rank r's
+ * buffer holds source rank i's tokens from rank_prefix_matrix[i-1][r] on,
+ * in token order, and the combine sums the rows the ranks return (the
+ * experts of a rank weight their outputs before returning them).  It is the
+ * per-expert pipeline run on per-slot destination-rank ids, with "experts"
+ * = ranks (E' = R, one per rank):
+ *   1. ep_rank_ids(topk_idx, ...)             -> rank_ids [R, T_r, k]
+ *   2. ep_get_dispatch_layout(rank_ids, R, T_r, k, E' = R, ...)
+ *        num_tokens_per_expert' = num_tokens_per_rank, slot_rank' = each
+ *        token's position among source rank i's tokens for r
+ *   3. ep_notify_dispatch(..., E' = R, expert_alignment 1, ...)
+ *        rank_prefix_matrix as for the per-expert layout; expert_prefix'
+ *        [i][r] = rank_prefix_matrix[i-1][r]; psum'[r] = {0, total};
+ *        num_worst_tokens caps received TOKENS per rank (cap_rows = it)
+ *   4. ep_dispatch(x, rank_ids, slot_rank', expert_prefix', psum', E' = R,
+ *        fp8_mode, cap_rows, ...) -> recv_x [R, cap_rows, H] (+ scales),
+ *        recv_src_idx, combine_idx [R, T_r, k]: r*cap_rows + row at the
+ *        token's first slot on r, -1 at its other slots
+ *   5. ep_rank_recv_topk(...)  -> each received row's local top-k ids/weights
+ *   6. ep_rank_combine(y, combine_idx, ...) -> out [R, T_r, H] bf16 */
+
+/* Per-slot destination rank: rank_ids[i][t][j] = topk_idx[i][t][j] / E_l
+ * when slot j is token t's first slot whose expert is on that rank, else -1
+ * (unused slot, or a rank the token already reached at an earlier slot).
+ * Invalid ids (outside [-1, E)) set EP_ERR_INVALID_ARG in *status and give -1.
+ * rank_ids: int64 [R, T_r, k], caller-owned device memory. */
+int ep_rank_ids(const int64_t* topk_idx, int R, int T_r, int k, int E, int64_t* rank_ids,
+                int32_t* status, void* stream);
+
+/* For every received row of the once-per-rank layout, the local view of
+ * its token's top-k: recv_topk_idx[r][row][j] = topk_idx[t][j] - r*E_l when
+ * that expert is on rank r, else -1; recv_topk_weights[r][row][j] = its
+ * weight, else 0.  combine_idx as returned by step 4 above.  Rows holding
+ * no token are left untouched.
+ *   recv_topk_idx     int64 [R, cap_rows, k]
+ *   recv_topk_weights fp32  [R, cap_rows, k] */
+int ep_rank_recv_topk(const int64_t* topk_idx, const float* topk_weights,
+                      const int32_t* combine_idx, int R, int T_r, int k, int E, int64_t cap_rows,
+                      int64_t* recv_topk_idx, float* recv_topk_weights, int32_t* status,
+                      void* stream);
+
+/* Rank-level combine (§2.3, dispatch walked backwards):
+ *   out[t][:] = bf16_rn( fp32 sum, from +0 in slot order, of y[f_j][:] over
+ *               the slots with f_j = combine_idx[t][j] >= 0 )
+ * one row per destination rank the token reached, each already weighted by
+ * that rank's experts.  y [R, cap_rows, H] bf16, out [R, T_r, H] bf16. */
+int ep_rank_combine(const void* y, const int32_t* combine_idx, int R, int T_r, int H, int k,
+                    int64_t cap_rows, void* out, int32_t* status, void* stream);
+
 /* clean_low_latency_buffer (§1.2): zero recv_count [R, E_l] (may be NULL)
  * and the workspace (may be NULL), stream-ordered.  Required once before a
  * workspace's first use and after any call that reported EP_ERR_TIMEOUT or
