@@ -446,51 +446,52 @@ __global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterPar
 // scatter, FP8 quantisation and the column-major scales.  One CTA per SM;
 // the batch's (token, 1024-channel piece) units are split evenly over the
 // CTAs (a CTA's "own" tokens are those it holds a piece of), and every CTA
-//   0. loads the ids it needs: CTA j < num_chunks those of the j-th chunk of
-//      1024 ids (in (rank, token, slot) order), every CTA those from the
-//      start of the chunk holding its first own id to its last own id;
-//   1. histograms its chunk and publishes it as tagged 64-bit words (launch
-//      epoch in the high half: a reader needs no flag and no fence), counts
-//      its partial prefix and keeps its own ids;
-//   2. adds the histograms of the chunks before its own (re-reading a word
-//      until it carries this launch's tag), which gives, per expert, the
-//      slots that precede its own range; ranks its own slots in order
-//      (equal-key lane masks), which gives each slot's packed row -- the
-//      global exclusive count of its expert (§1.2, §3.2) -- and writes
-//      combine_idx and src_info for the tokens whose first piece it holds
-//      (the CTA holding the last token writes recv_count);
-//   3. only now bulk-loads the rest of its x pieces -- one per unit warp
-//      went out with the ids -- (a read issued while ~30 MB of bulk loads are queued
-//      waits behind them, and steps 0-2 are a chain of such reads).
-//      bf16: as each lands, its k bulk stores go out.  FP8: warps 0..11 own
-//      the units, quantise each in place as it lands (staging the token's
+//   0. loads every id from the first up to its last own id (in (rank,
+//      token, slot) order), then bulk-loads all of its x pieces behind them;
+//   1. counts, per expert, the ids before its own range -- the slots that
+//      precede its own range in the packed order -- and keeps its own ids,
+//      so it needs nothing from any other CTA to place its rows;
+//   2. its 4 rank warps rank the own slots in order (equal-key lane masks),
+//      which gives each slot's packed row -- the global exclusive count of
+//      its expert (§1.2, §3.2) -- and write combine_idx and src_info for the
+//      tokens whose first piece the CTA holds (the CTA holding the last token
+//      has seen every id and writes recv_count);
+//   3. bf16: as each piece lands, its k bulk stores go out.  FP8: warps 0..11
+//      own the units, quantise each in place as it lands (staging the token's
 //      block scales row-major) and mark it on a per-unit mbarrier; warps
-//      12..15 issue each unit's k bulk stores the moment it is marked, so
-//      the store stream starts with the first quantised piece;
+//      12..15 (the rank warps) issue each unit's k bulk stores the moment it
+//      is marked and its rows are known;
 //   4. the unit warps (bf16: all warps) arrive at a grid barrier (workspace
 //      counter), wait for every CTA, and write the per-expert outputs of
 //      the experts e = cta + n * grid while the stores drain: layout_range
 //      from the sources of their rows (sorted by token, so each rank is one
 //      run) and (FP8) the column-major scales, coalesced along rows.
-// All CTAs are resident at once (one per SM, grid = SM count), so the waits
-// on other CTAs (chunk words, the barrier) end; every wait is bounded anyway
-// and gives up with EP_ERR_TIMEOUT.
+// The id scan is redundant across CTAs (CTA j reads ~j/grid of the ids, from
+// L2 after the first touch) but takes no round trip through another CTA: an
+// exchange of per-chunk counts, read while the x pieces are queued, made
+// every CTA wait for the slowest and for the x queue.
+// All CTAs are resident at once (one per SM, grid = SM count), so the wait
+// at the grid barrier ends; every wait is bounded anyway and gives up with
+// EP_ERR_TIMEOUT.
 
 constexpr int kFusedWarps = 16;
 constexpr int kQuantWarps = 12;          // FP8: warps owning (loading, quantising) units; the
                                          // other 4 issue the bulk stores as units are quantised
 constexpr int kFusedMaxPerWarp = 8;      // units per warp
 constexpr int kFusedPiece = 1024;        // channels per unit
-constexpr int kEarlyUnits = 1;           // units per warp loaded at kernel start
-constexpr int kRankWarps = 8;            // warps that rank a CTA's own slots
-constexpr int kRankIdsPerLane = 4;
+constexpr int kEarlyUnits = 1;           // units per warp loaded with the ids; the rest once
+                                         // the ids have landed
+constexpr int kRankWarps = 4;            // the last warps: rank the CTA's own slots (FP8: the
+                                         // store warps)
+constexpr int kRankIdsPerLane = 8;
 constexpr int kMaxOwnIds = kRankWarps * kWarp * kRankIdsPerLane;
-constexpr int kFusedChunkIds = 1024;     // ids per published histogram
+constexpr int kScanIdsPerThread = 32;    // ids a thread has in flight per pass of the id scan
+constexpr int kFusedMaxIds = 4 * kFusedWarps * kWarp * kScanIdsPerThread;   // at most 4 passes
 constexpr int kFusedBarBytes = 2 * kFusedWarps * kFusedMaxPerWarp * 8;   // load + quantised barriers
 constexpr size_t kFusedSmemCap = 225 * 1024;
+static_assert(kRankWarps == kFusedWarps - kQuantWarps, "FP8: the rank warps are the store warps");
 constexpr int kCtlArrive = 8;            // workspace control words of this kernel
 constexpr int kCtlExit = 9;
-constexpr int kCtlEpoch = 10;
 
 // Wait (bounded, kWaitNs) until a grid counter reaches n; false on timeout.
 __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t n) {
@@ -519,8 +520,6 @@ struct FusedParams {
   uint8_t* scale_rows;       // [T][scale_row_bytes] staged per-token scales
   int scale_row_bytes;
   uint32_t* ctl;             // workspace control words
-  uint64_t* chunk_hist;      // [num_chunks][E] (launch tag << 32) | count
-  int num_chunks;
   int32_t* status;
   // geometry
   int Hp, P;
@@ -636,8 +635,7 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   constexpr bool kFp8 = kMode != EP_FP8_NONE;
   constexpr int kEs = kMode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
   constexpr int kThreads = kFusedWarps * kWarp;
-  __shared__ uint32_t s_epoch;
-  __shared__ int s_ok, s_units_ok, s_passed;
+  __shared__ int s_units_ok, s_passed;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -658,8 +656,7 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   uint64_t* qbars = reinterpret_cast<uint64_t*>(smem + p.slot_area) + kFusedWarps * kFusedMaxPerWarp;
   int32_t* s_P = reinterpret_cast<int32_t*>(smem + p.slot_area + kFusedBarBytes);   // [E]
   int32_t* s_cnt = s_P + p.E;                    // [kRankWarps][E]
-  int32_t* s_H = s_cnt + kRankWarps * p.E;       // [E] histogram of chunk `cta`
-  int32_t* s_own = s_H + p.E;                    // [own_cap] own ids
+  int32_t* s_own = s_cnt + kRankWarps * p.E;     // [own_cap] own ids
   int32_t* s_f = s_own + p.own_cap;              // [own_cap] their packed rows
   int32_t* s_lo = s_f + p.own_cap;               // [nA][R + 1] first row of every rank
   auto unit_slot = [&](int32_t m) { return slots + (size_t)(warp + m * kOwnWarps) * p.slot_bytes; };
@@ -669,44 +666,34 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
     *pc = u - *g * p.P;
   };
 
-  // own token range [ga, gb) and the ids this CTA reads
+  // own token range [ga, gb) and its ids [own_lo, own_hi)
   const int32_t ga = u0 / p.P;
   const int32_t gb = u1 > u0 ? (u1 - 1) / p.P + 1 : ga;
   const int32_t own_lo = ga * p.k;
   const int32_t own_hi = gb * p.k;
   const int32_t own_n = own_hi - own_lo;
-  const int32_t J = own_lo / kFusedChunkIds;        // chunks wholly before the own range
-  const int32_t scan_lo = J * kFusedChunkIds;       // counted here: [scan_lo, own_hi)
-  const bool chunk_cta = cta < p.num_chunks;
-  const int32_t ch_lo = cta * kFusedChunkIds;
-  const int32_t ch_hi = min(ch_lo + kFusedChunkIds, p.n_ids);
   const int64_t last_first = (int64_t)(p.T - 1) * p.P;
   const bool totals = last_first >= u0 && last_first < u1;   // sees every id: writes recv_count
+  const int32_t scan_hi = own_n > 0 ? own_hi : 0;   // a CTA without units reads no ids
 
-  // ---- 0. the ids: they are on the critical path, so they go out before any
-  //      bulk load of x (which would queue them behind ~30 MB of reads)
-  constexpr int kScanPairs = 2;                     // 16-byte id loads per thread per pass
-  static_assert(2 * kThreads >= kFusedChunkIds, "one 16-byte load per thread covers a chunk");
-  longlong2 vc = make_longlong2(-1, -1);
+  // ---- 0. every id up to the end of the own range goes out first: the CTA
+  //      counts the ids before its range itself (their per-expert counts are
+  //      its prefix), so it waits for no other CTA.  Only kEarlyUnits pieces
+  //      per warp follow them now: ~30 MB of reads in flight grid-wide would
+  //      hold the ids back by microseconds.
+  constexpr int kScanPairs = kScanIdsPerThread / 2;   // 16-byte id loads per thread per pass
+  constexpr int kPassIds = 2 * kThreads * kScanPairs;
   longlong2 vs[kScanPairs];
-  {
-    const int32_t q = ch_lo + 2 * tid;
-    if (chunk_cta && q + 1 < ch_hi) vc = ld_nc_i64x2(p.topk_idx + q);
-    else if (chunk_cta && q < ch_hi) vc.x = __ldg(p.topk_idx + q);
-  }
   auto load_scan = [&](int32_t base) {
 #pragma unroll
     for (int u = 0; u < kScanPairs; ++u) {
       const int32_t q = base + 2 * (tid + u * kThreads);
       vs[u] = make_longlong2(-1, -1);
-      if (q + 1 < own_hi) vs[u] = ld_nc_i64x2(p.topk_idx + q);
-      else if (q < own_hi) vs[u].x = __ldg(p.topk_idx + q);
+      if (q + 1 < scan_hi) vs[u] = ld_nc_i64x2(p.topk_idx + q);
+      else if (q < scan_hi) vs[u].x = __ldg(p.topk_idx + q);
     }
   };
-  load_scan(scan_lo);
-  // the first kEarlyUnits pieces of every warp go out right behind the ids
-  // (a small queue of loads: the id chain barely notices it), so stores can
-  // start the moment the ranks are known
+  load_scan(0);
   auto load_unit = [&](int32_t m) {
     int32_t g;
     int pc;
@@ -725,128 +712,83 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
     fence_barrier_init();
     for (int32_t m = 0; m < min(nm, kEarlyUnits); ++m) load_unit(m);
   }
-  for (int i = tid; i < (2 + kRankWarps) * p.E; i += kThreads) s_P[i] = 0;   // s_P, s_cnt, s_H
-  if (tid == 0) {
-    s_epoch = ld_relaxed_u32(&p.ctl[kCtlEpoch]);
-    s_units_ok = 1;
-  }
+  for (int i = tid; i < (1 + kRankWarps) * p.E; i += kThreads) s_P[i] = 0;   // s_P, s_cnt
+  if (tid == 0) s_units_ok = 1;
   __syncthreads();
-  const uint32_t tag = s_epoch + 1u;
 
-  // ---- 1. the chunk histogram (published), the partial prefix and own ids
+  // ---- 1. per-expert counts of the ids before the own range, and the own ids
   {
     bool bad = false;
-    auto valid = [&](int64_t id) {
-      if (id >= 0 && id < p.E) return (int)id;
-      bad |= (id != -1);
-      return -1;
-    };
-    if (chunk_cta) {
-      const int e0 = valid(vc.x), e1 = valid(vc.y);
-      if (e0 >= 0) atomicAdd(&s_H[e0], 1);
-      if (e1 >= 0) atomicAdd(&s_H[e1], 1);
-    }
     auto count = [&](int32_t q, int64_t id) {
-      const int e = valid(id);
+      int e = -1;
+      if (id >= 0 && id < p.E) e = (int)id;
+      else bad |= (id != -1);
       if (q < own_lo) {
         if (e >= 0) atomicAdd(&s_P[e], 1);
       } else {
         s_own[q - own_lo] = e;
       }
     };
-    for (int32_t base = scan_lo; base < own_hi; base += 2 * kThreads * kScanPairs) {
-      if (base > scan_lo) load_scan(base);
+    for (int32_t base = 0; base < scan_hi; base += kPassIds) {
+      if (base > 0) load_scan(base);
 #pragma unroll
       for (int u = 0; u < kScanPairs; ++u) {
         const int32_t q = base + 2 * (tid + u * kThreads);
-        if (q < own_hi) count(q, vs[u].x);
-        if (q + 1 < own_hi) count(q + 1, vs[u].y);
+        if (q < scan_hi) count(q, vs[u].x);
+        if (q + 1 < scan_hi) count(q + 1, vs[u].y);
       }
     }
     if (bad) set_status(p.status, EP_ERR_INVALID_ARG);
   }
   __syncthreads();
-  if (chunk_cta)   // tagged words: a reader sees the old word or the whole new one
-    for (int e = tid; e < p.E; e += kThreads)
-      st_relaxed_u64(&p.chunk_hist[(size_t)cta * p.E + e], ((uint64_t)tag << 32) | (uint32_t)s_H[e]);
-  if (tid == 0) s_ok = 1;
-  __syncthreads();
+  if (nm > 0 && lane == 0)   // the ids are in: the rest of the pieces may queue now
+    for (int32_t m = min(nm, kEarlyUnits); m < nm; ++m) load_unit(m);
 
-  // ---- 2. prefix of the chunks before the own range (their tagged words,
-  //      all loads of a pass in flight, a word re-read until its tag is this
-  //      launch's), then the own ranks
-  {
-    constexpr int kHistLoads = 8;
-    const int32_t n = J * p.E;
-    for (int32_t i0 = 0; i0 < n; i0 += kThreads * kHistLoads) {
-      uint64_t w[kHistLoads];
-#pragma unroll
-      for (int u = 0; u < kHistLoads; ++u) {
-        const int32_t i = i0 + u * kThreads + tid;
-        w[u] = i < n ? ld_relaxed_u64(&p.chunk_hist[i]) : ((uint64_t)tag << 32);
-      }
-#pragma unroll
-      for (int u = 0; u < kHistLoads; ++u) {
-        const int32_t i = i0 + u * kThreads + tid;
-        if ((uint32_t)(w[u] >> 32) != tag) {
-          const uint64_t t0 = globaltimer_ns();
-          do {
-            __nanosleep(32);
-            w[u] = ld_relaxed_u64(&p.chunk_hist[i]);
-            if (globaltimer_ns() - t0 > kWaitNs) {
-              set_status(p.status, EP_ERR_TIMEOUT);
-              s_ok = 0;
-              w[u] = (uint64_t)tag << 32;
-            }
-          } while ((uint32_t)(w[u] >> 32) != tag);
-        }
-        const int32_t c = (int32_t)(uint32_t)w[u];
-        if (c != 0) atomicAdd(&s_P[i % p.E], c);
-      }
-    }
-  }
-  __syncthreads();
-  const int per = ((own_n + kRankWarps * kWarp - 1) / (kRankWarps * kWarp)) * kWarp;
-  int my_rank[kRankIdsPerLane];
-  if (warp < kRankWarps) {
+  // ---- 2. the rank warps rank the own slots among themselves (ballots), turn
+  //      the per-warp counts into warp starts after the prefix and write the
+  //      own rows; the FP8 unit warps meanwhile quantise (step 3)
+  const int rw = warp - (kFusedWarps - kRankWarps);   // rank warp index (< 0: not one)
+  if (rw >= 0) {
+    constexpr int kRankThreads = kRankWarps * kWarp;
+    const int rt = tid - (kFusedWarps - kRankWarps) * kWarp;
+    const int per = ((own_n + kRankThreads - 1) / kRankThreads) * kWarp;
+    int my_rank[kRankIdsPerLane];
 #pragma unroll
     for (int u = 0; u < kRankIdsPerLane; ++u) {
       my_rank[u] = 0;
       if (u * kWarp < per) {
-        const int q = warp * per + u * kWarp + lane;
+        const int q = rw * per + u * kWarp + lane;
         const int e = q < own_n ? s_own[q] : -1;
         const uint32_t peers = peers_mask(e, p.nbits);
         int r = 0;
-        if (e >= 0) r = s_cnt[warp * p.E + e] + __popc(peers & lanemask_lt());
+        if (e >= 0) r = s_cnt[rw * p.E + e] + __popc(peers & lanemask_lt());
         __syncwarp();
-        if (e >= 0 && (__ffs(peers) - 1) == lane) s_cnt[warp * p.E + e] += __popc(peers);
+        if (e >= 0 && (__ffs(peers) - 1) == lane) s_cnt[rw * p.E + e] += __popc(peers);
         __syncwarp();
         my_rank[u] = r;
       }
     }
-  }
-  __syncthreads();
-  for (int e = tid; e < p.E; e += kThreads) {   // per-warp counts -> warp starts
-    int run = s_P[e];
+    named_barrier_sync(2, kRankThreads);
+    for (int e = rt; e < p.E; e += kRankThreads) {   // per-warp counts -> warp starts
+      int run = s_P[e];
 #pragma unroll
-    for (int w = 0; w < kRankWarps; ++w) {
-      const int c = s_cnt[w * p.E + e];
-      s_cnt[w * p.E + e] = run;
-      run += c;
+      for (int w = 0; w < kRankWarps; ++w) {
+        const int c = s_cnt[w * p.E + e];
+        s_cnt[w * p.E + e] = run;
+        run += c;
+      }
+      if (totals) p.recv_count[e] = run;
     }
-    if (totals) p.recv_count[e] = run;
-  }
-  __syncthreads();
-  if (warp < kRankWarps) {
+    named_barrier_sync(2, kRankThreads);
 #pragma unroll
     for (int u = 0; u < kRankIdsPerLane; ++u) {
       if (u * kWarp < per) {
-        const int q = warp * per + u * kWarp + lane;
+        const int q = rw * per + u * kWarp + lane;
         if (q < own_n) {
           const int e = s_own[q];
           int32_t f = -1;
-          if (e >= 0 && s_ok) {
-            const int64_t row = (int64_t)s_cnt[warp * p.E + e] + my_rank[u];
+          if (e >= 0) {
+            const int64_t row = (int64_t)s_cnt[rw * p.E + e] + my_rank[u];
             if (row < p.seg_rows) f = (int32_t)((int64_t)e * p.seg_rows + row);
             else set_status(p.status, EP_ERR_CAPACITY);
           }
@@ -859,33 +801,36 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
         }
       }
     }
+    // FP8: the src_info writes are released to the unit warps' grid-barrier
+    // arrival (barrier 3); the rows are complete for the store warps (barrier 2)
+    if (kFp8) named_barrier_arrive(3, kThreads);
+    named_barrier_sync(2, kRankThreads);
   }
-  // the rest of this CTA's source pieces in flight, only now: a read issued
-  // while ~30 MB of bulk loads are queued waits behind them, and the steps
-  // above are one chain of such reads
-  if (nm > 0 && lane == 0) {
-    for (int32_t m = min(nm, kEarlyUnits); m < nm; ++m) load_unit(m);
-  }
-  __syncthreads();
+  if (!kFp8) __syncthreads();   // bf16: every warp stores, with the rows
 
-  // ---- 3. bf16: every warp stores its units as they land.  FP8: the unit
-  //      warps quantise their units in place as they land (staging each
-  //      token's scales row-major) and mark each one quantised; the store
-  //      warps issue each unit's k bulk stores as soon as it is marked
+  // ---- 3. FP8: the unit warps quantise their units in place as they land
+  //      (staging each token's scales row-major) and mark each one; the store
+  //      warps issue each unit's k bulk stores as soon as it is marked.  bf16:
+  //      every warp stores its units as they land.
+  // A unit that never landed: report it, wait (bounded) for the loads still
+  // in flight and release the store warps from unit m on.
+  auto fail_from = [&](int32_t m) {
+    set_status(p.status, EP_ERR_TIMEOUT);
+    s_units_ok = 0;
+    __syncwarp();
+    if (lane == 0)
+      for (int32_t r = m; r < nm; ++r) {
+        mbar_wait_bounded(&bars[r], 0);
+        if (kFp8) mbar_arrive(&qbars[warp + r * kOwnWarps]);
+      }
+  };
   const int64_t row_bytes = kFp8 ? (int64_t)p.H : (int64_t)p.H * 2;
   const int32_t n_own_units = u1 - u0;
   if (!kFp8 || warp < kQuantWarps) {
     for (int32_t m = 0; m < nm; ++m) {
       const bool landed = mbar_wait_bounded(&bars[m], 0);
       if (!__all_sync(0xffffffffu, landed)) {
-        set_status(p.status, EP_ERR_TIMEOUT);
-        s_units_ok = 0;
-        if (lane == 0) {   // wait (bounded) for what is still in flight; release the store warps
-          for (int32_t r = m; r < nm; ++r) {
-            mbar_wait_bounded(&bars[r], 0);
-            if (kFp8) mbar_arrive(&qbars[warp + r * kOwnWarps]);
-          }
-        }
+        fail_from(m);
         break;
       }
       int32_t g;
@@ -966,7 +911,10 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
       if (kFp8) named_barrier_sync(1, kGroup);
       else __syncthreads();
     };
-    sync();   // the group's staged scales (and src_info, written before) are out
+    // the group's staged scales and (FP8: the rank warps arrive at barrier 3
+    // once their src_info is written) every row source are out
+    if (kFp8) named_barrier_sync(3, kThreads);
+    else sync();
     if (tid == 0) {   // the group leader alone writes s_passed
       __threadfence();
       int passed = 1;
@@ -981,37 +929,30 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
       __threadfence();
       s_passed = passed;
     }
-    sync();   // s_ok (settled before step 3) and s_passed are read by the whole group
-    if (s_ok && s_passed) fused_expert_outputs<kFp8, kEs>(p, cta, grid, tid, kGroup, s_P, s_lo, sync);
+    sync();   // s_passed is read by the whole group
+    if (s_passed) fused_expert_outputs<kFp8, kEs>(p, cta, grid, tid, kGroup, s_P, s_lo, sync);
   }
   __syncthreads();
   pdl_launch_dependents();   // a dependent combine may take its place as this drains
-  if (tid == 0) {   // the last CTA out resets the barrier and moves the epoch on
+  if (tid == 0) {   // the last CTA out resets the barrier
     const uint32_t d = atomicAdd(&p.ctl[kCtlExit], 1u);
     if (d == (uint32_t)grid - 1) {
       p.ctl[kCtlArrive] = 0;
       p.ctl[kCtlExit] = 0;
-      p.ctl[kCtlEpoch] = s_epoch + 1u;
     }
   }
   tma_wait_all();   // the bulk stores have read their slots before the CTA leaves
 }
 
 static size_t fused_smem(const FusedParams& p) {
-  const size_t tables = (size_t)p.E * (2 + kRankWarps) + 2 * (size_t)p.own_cap +
+  const size_t tables = (size_t)p.E * (1 + kRankWarps) + 2 * (size_t)p.own_cap +
                         (size_t)p.nA * (p.R + 1);
   return (size_t)p.slot_area + kFusedBarBytes + tables * sizeof(int32_t);
 }
 
-// Workspace bytes of the fused path's chunk histograms (after the FP8 staging).
-static size_t fused_region_bytes(int R, int T_r, int k, int E) {
-  const int64_t chunks = ((int64_t)R * T_r * k + kFusedChunkIds - 1) / kFusedChunkIds;
-  return (size_t)((chunks * E * 8 + 255) / 256 * 256);
-}
-
 // Geometry of the fused path, or false when the batch does not fit it.
 static bool plan_fused(FusedParams& p, int grid) {
-  if ((int64_t)p.T * p.k >= INT32_MAX || p.T == 0) return false;
+  if ((int64_t)p.T * p.k > kFusedMaxIds || p.T == 0) return false;
   const int hp = std::min(p.H, kFusedPiece);
   p.Hp = hp;
   p.P = (p.H + hp - 1) / hp;
@@ -1026,8 +967,6 @@ static bool plan_fused(FusedParams& p, int grid) {
   const int64_t own = (own_tokens * p.k + kWarp - 1) / kWarp * kWarp;
   if (own > kMaxOwnIds) return false;
   p.own_cap = (int)own;
-  p.num_chunks = (int)(((int64_t)p.T * p.k + kFusedChunkIds - 1) / kFusedChunkIds);
-  if (p.num_chunks > grid) return false;
   p.nA = (p.E + grid - 1) / grid;
   if (p.nA > kFusedWarps * kWarp) return false;
   p.nbits = key_bits(p.E);
@@ -1313,16 +1252,11 @@ static uint8_t* scale_staging(void* ws, int R, int T_r, int k, int E) {
   return static_cast<uint8_t*>(ws) + layout_region_bytes(R, T_r, k, E);
 }
 
-static uint8_t* fused_region(void* ws, int R, int T_r, int k, int E, int H) {
-  return scale_staging(ws, R, T_r, k, E) + staging_bytes(R, T_r, H);
-}
-
 }  // namespace ep
 
 extern "C" size_t ep_workspace_size(int R, int T_r, int k, int E, int H) {
   if (R <= 0 || k <= 0 || k > ep::kMaxK || E <= 0 || T_r < 0 || H <= 0) return 0;
-  return ep::layout_region_bytes(R, T_r, k, E) + ep::staging_bytes(R, T_r, H) +
-         ep::fused_region_bytes(R, T_r, k, E);
+  return ep::layout_region_bytes(R, T_r, k, E) + ep::staging_bytes(R, T_r, H);
 }
 
 extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t* slot_rank,
@@ -1434,10 +1368,6 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
     fp.scale_rows = scale_rows;
     fp.scale_row_bytes = fp8 ? ep::scale_row_bytes(H, es) : 0;
     fp.ctl = static_cast<uint32_t*>(workspace);
-    uint8_t* fr = ep::fused_region(workspace, R, T_r, k, E, H);
-    const int64_t chunks = ((int64_t)R * T_r * k + ep::kFusedChunkIds - 1) / ep::kFusedChunkIds;
-    (void)chunks;
-    fp.chunk_hist = reinterpret_cast<uint64_t*>(fr);
     fp.status = status;
     fp.fp8 = fp8;
     if (ep::plan_fused(fp, grid))

@@ -121,6 +121,11 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void named_barrier_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+// Arrive at barrier `id` without waiting: this thread's earlier memory
+// accesses are performed for the threads that wait there (bar.sync id, n).
+__device__ __forceinline__ void named_barrier_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

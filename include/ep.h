@@ -69,8 +69,8 @@ extern "C" {
  * ep_ll_dispatch need for problems up to (R, T_r, k, E, H); 0 for invalid
  * sizes.  The workspace holds the cross-block prefix (decoupled look-back)
  * state of the layout kernels, the per-token FP8 scales staged between the
- * scatter and the column-major scale pass, and the per-chunk histograms and
- * barrier words of the single-launch low-latency path.  It must be zeroed once with
+ * scatter and the column-major scale pass, and the grid-barrier words of the
+ * single-launch low-latency path.  It must be zeroed once with
  * ep_clean_ll_buffer before its first use, after which every call leaves it
  * ready for the next.  Calls that share one workspace must be ordered on
  * one stream (overlapping calls race).  16-byte aligned. */

@@ -157,9 +157,9 @@ def test_single_launch_path_reports_an_uncleaned_workspace():
 
 @pytest.mark.parametrize("fp8_mode", [0, 1, 2])
 def test_single_launch_path_repeated_calls_on_one_workspace(fp8_mode):
-    """The single-launch path moves its launch epoch on at every call; five
-    calls in a row on one workspace (different routings) must each match
-    the oracle."""
+    """The single-launch path resets its grid-barrier words at the end of
+    every call; five calls in a row on one workspace (different routings)
+    must each match the oracle."""
     base = synth.scaled(synth.WORKLOADS["decode"], T_r=24, H=1024, fp8_mode=fp8_mode)
     ws = ep.alloc_workspace(base.R, base.T_r, base.k, base.E, base.H)
     for seed in range(5):
@@ -174,8 +174,8 @@ def test_low_latency_dispatch_and_combine_replay_as_a_cuda_graph(fp8_mode):
     """The low-latency path has no host round trip, so a dispatch + combine
     pair can be captured once into a CUDA graph and replayed: every replay
     with new inputs copied into the captured buffers must match the oracle
-    (the single-launch kernel's epoch and barrier words advance inside the
-    graph, as between eager calls)."""
+    (the single-launch kernel's barrier words are reset inside the graph, as
+    between eager calls)."""
     w = synth.scaled(synth.WORKLOADS["decode"], T_r=32, H=1024, fp8_mode=fp8_mode)
     S = w.R * w.max_tokens_per_rank
     x_dev, _, idx_dev, _, wts_dev, _ = inputs(w)
