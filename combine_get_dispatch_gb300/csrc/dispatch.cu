@@ -879,20 +879,29 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
       }
     }
   } else {
-    // FP8 store warps: units in slot order, each once it is quantised
-    for (int32_t q = warp - kQuantWarps; q < n_own_units; q += kFusedWarps - kQuantWarps) {
-      const bool ready = mbar_wait_bounded(&qbars[q], 0);
+    // FP8 store warps: units in slot order, each once it is quantised.  A
+    // warp takes G = 32 / k units at a time, one lane per (unit, slot): a
+    // thread's bulk copies go out one after another, so the number of
+    // issuing threads, not the warps, sets how many 1 KB pieces are in flight.
+    const int G = kWarp / p.k;
+    const int32_t gq = lane / p.k;   // this lane's unit within the group
+    const int j = lane - gq * p.k;   // and its slot
+    constexpr int kStoreWarps = kFusedWarps - kQuantWarps;
+    for (int32_t qb = (warp - kQuantWarps) * G; qb < n_own_units; qb += kStoreWarps * G) {
+      const int32_t q = qb + gq;
+      const bool mine = gq < G && q < n_own_units;
+      const bool ready = mine ? mbar_wait_bounded(&qbars[q], 0) : true;
       if (!__all_sync(0xffffffffu, ready)) {
         set_status(p.status, EP_ERR_TIMEOUT);
         break;
       }
       if (!s_units_ok) continue;
-      const int32_t u = u0 + q;
-      const int32_t g = u / p.P;
-      const int pc = u - g * p.P;
-      const int hc = min(p.Hp, p.H - pc * p.Hp);
-      if (lane < p.k) {
-        const int32_t f = s_f[(g - ga) * p.k + lane];
+      if (mine) {
+        const int32_t u = u0 + q;
+        const int32_t g = u / p.P;
+        const int pc = u - g * p.P;
+        const int hc = min(p.Hp, p.H - pc * p.Hp);
+        const int32_t f = s_f[(g - ga) * p.k + j];
         if (f >= 0)
           tma_store_1d(p.recv_x + f * row_bytes + (int64_t)pc * p.Hp,
                        slots + (size_t)q * p.slot_bytes, (uint32_t)hc);
