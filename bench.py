@@ -13,6 +13,8 @@ run under "workloads".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workloads decode,prefill,skewed,large]
+  python bench.py --sm-sweep 8,16,32,64,152 [--workloads ...]   (GB/s per SM
+                  under an SM budget; one line per workload and budget)
 
 With N > 1 (torchrun) every rank runs an independent replica (the emulated
 ranks live inside one GPU; there is no data-path collective): weak scaling,
@@ -52,6 +54,9 @@ def parse_args(argv=None):
                     help="override T_r of every selected workload (profiling only)")
     ap.add_argument("--no-combine", action="store_true",
                     help="dispatch only, no expert-output buffer (profiling only)")
+    ap.add_argument("--sm-sweep", default="",
+                    help="comma list of SM budgets (ep_set_num_sms): print one line per "
+                         "workload and budget with GB/s per SM instead of the headline line")
     return ap.parse_args(argv)
 
 
@@ -451,6 +456,49 @@ def run_reference(args, rank, world):
     return 0
 
 
+def run_sm_sweep(args, local_rank):
+    """Dispatch / combine bandwidth per SM under an SM budget (the kernels
+    confined to n SMs), one JSON line per (workload, budget): the per-SM
+    read and write rates that size a budget (num_sms = traffic / per-SM
+    rate, the bandwidth model of the DeepEP article's §4.6)."""
+    import torch
+
+    from combine_get_dispatch_gb300 import ep, synth
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ep.load()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    budgets = [int(b) for b in args.sm_sweep.split(",") if b.strip()]
+    try:
+        for name in [n.strip() for n in args.workloads.split(",") if n.strip()]:
+            w = synth.WORKLOADS[name]
+            runner = Runner(w, dev)
+            row_in = 2 * w.H
+            row_out = (2 * w.H if w.fp8_mode == 0
+                       else w.H + (w.H // 128) * (4 if w.fp8_mode == 1 else 1))
+            d_rd, d_wr = w.T * row_in, runner.rows * row_out
+            c_rd, c_wr = runner.rows * 2 * w.H, w.T * 2 * w.H
+            for b in budgets:
+                ep.ep_set_num_sms(b)
+                n = ep.ep_get_num_sms()
+                res = measure(runner, args.steps, args.warmup, 1, flush, e2e=False)
+                d_s, c_s = res["dispatch_ms"] * 1e-3, res["combine_ms"] * 1e-3
+                print(json.dumps({
+                    "sm_sweep": name, "num_sms": n,
+                    "dispatch_us": round(d_s * 1e6, 2), "combine_us": round(c_s * 1e6, 2),
+                    "dispatch_gbs": round((d_rd + d_wr) / d_s / 1e9, 1),
+                    "combine_gbs": round((c_rd + c_wr) / c_s / 1e9, 1),
+                    "dispatch_read_gbs_per_sm": round(d_rd / d_s / 1e9 / n, 2),
+                    "dispatch_write_gbs_per_sm": round(d_wr / d_s / 1e9 / n, 2),
+                    "combine_read_gbs_per_sm": round(c_rd / c_s / 1e9 / n, 2),
+                    "combine_write_gbs_per_sm": round(c_wr / c_s / 1e9 / n, 2)}), flush=True)
+            del runner
+            torch.cuda.empty_cache()
+    finally:
+        ep.ep_set_num_sms(0)
+    return 0
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -556,6 +604,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, rank, world)
+        if args.sm_sweep:
+            return run_sm_sweep(args, local_rank) if rank == 0 else 0
         return run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:

@@ -1,5 +1,6 @@
 // api.cu -- host-side helpers and the small entry points of libep.
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <set>
@@ -30,6 +31,16 @@ int num_sms() {
   }
   return cached[dev];
 }
+
+static std::atomic<int> g_sm_budget{0};   // 0: every SM
+
+int grid_cap(int ctas_per_sm) {
+  const int sms = num_sms();
+  const int budget = g_sm_budget.load(std::memory_order_relaxed);
+  return budget > 0 ? std::min(budget, sms) : sms * ctas_per_sm;
+}
+
+bool sm_budget_set() { return g_sm_budget.load(std::memory_order_relaxed) > 0; }
 
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
@@ -86,6 +97,14 @@ extern "C" int ep_read_status(const int32_t* status, int32_t* host_value, void* 
   }
   return EP_OK;
 }
+
+extern "C" int ep_set_num_sms(int num_sms) {
+  if (num_sms < 0) return EP_ERR_INVALID_ARG;
+  ep_host::g_sm_budget.store(num_sms, std::memory_order_relaxed);
+  return EP_OK;
+}
+
+extern "C" int ep_get_num_sms(void) { return ep_host::grid_cap(1); }
 
 extern "C" uint64_t ep_launch_count(void) {
   return ep_host::g_launches.load(std::memory_order_relaxed);

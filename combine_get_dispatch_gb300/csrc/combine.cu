@@ -24,7 +24,8 @@
 
 namespace ep {
 
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = 256;   // two CTAs per SM; one CTA of twice that
+                                       // per SM under an SM budget
 
 struct CombineParams {
   const uint8_t* y;
@@ -38,15 +39,15 @@ struct CombineParams {
 };
 
 template <int kU, int kK>
-__global__ void __launch_bounds__(kCombineThreads, 2) k_combine(CombineParams p) {
+__global__ void __launch_bounds__(2 * kCombineThreads, 1) k_combine(CombineParams p) {
   constexpr int kSegC = kU * kWarp * 8;
   // launched as a programmatic dependent: the CTAs may be resident before
   // the kernel that wrote combine_idx (the dispatch) has finished
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const uint64_t pol = l2_policy_evict_first();   // every expert-output row is read once
-  const int64_t warp0 = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kCombineThreads) >> 5;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t row_bytes = (int64_t)p.H * 2;
 
   for (int64_t it = warp0; it < (int64_t)p.T * p.nseg; it += nwarps) {
@@ -123,11 +124,14 @@ static int launch_combine_t(const CombineParams& p, cudaStream_t stream) {
   q.nseg = (p.H + kSegC - 1) / kSegC;
   const int64_t items = q.T * q.nseg;
   if (items == 0) return EP_OK;
-  const int64_t want = (items + (kCombineThreads / kWarp) - 1) / (kCombineThreads / kWarp);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::num_sms() * 2));
+  // two CTAs per SM; under an SM budget one CTA of twice the threads on
+  // each budgeted SM (the same warps per SM, on fewer SMs)
+  const int threads = ep_host::sm_budget_set() ? 2 * kCombineThreads : kCombineThreads;
+  const int64_t want = (items + (threads / kWarp) - 1) / (threads / kWarp);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::grid_cap(2)));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kCombineThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -1064,11 +1064,14 @@ template <bool kLL, int kEs>
 __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColParams p) {
   if (kLL) {
     pdl_wait();   // the scatter's staged scales and row sources
-    const int64_t lim = min((int64_t)max(__ldg(&p.recv_count[blockIdx.x]), 0), p.seg_rows);
-    for (int64_t row = threadIdx.x; row < lim; row += kScaleColThreads) {
-      const int64_t f = (int64_t)blockIdx.x * p.seg_rows + row;
-      const int64_t src = __ldg(&p.src_idx[f]);
-      if (src >= 0 && src < p.T) scale_row_to_columns<kEs>(p, blockIdx.x, row, src);
+    const int64_t n_seg = p.n_rows / p.seg_rows;
+    for (int64_t e = blockIdx.x; e < n_seg; e += gridDim.x) {   // one expert per CTA pass
+      const int64_t lim = min((int64_t)max(__ldg(&p.recv_count[e]), 0), p.seg_rows);
+      for (int64_t row = threadIdx.x; row < lim; row += kScaleColThreads) {
+        const int64_t f = e * p.seg_rows + row;
+        const int64_t src = __ldg(&p.src_idx[f]);
+        if (src >= 0 && src < p.T) scale_row_to_columns<kEs>(p, e, row, src);
+      }
     }
     return;
   }
@@ -1136,11 +1139,11 @@ template <bool kLL, int kEs>
 static int launch_scale_columns_t(const ScaleColParams& p, cudaStream_t stream) {
   dim3 grid;
   if (kLL) {
-    grid = dim3((unsigned)(p.n_rows / p.seg_rows));
+    grid = dim3((unsigned)std::min<int64_t>(p.n_rows / p.seg_rows, ep_host::grid_cap(8)));
   } else {   // the valid rows are known only on the device: at most T * k
     const int64_t want = (p.T * 16 + kScaleColThreads - 1) / kScaleColThreads;
     grid = dim3((unsigned)std::max<int64_t>(
-        1, std::min<int64_t>(want, (int64_t)ep_host::num_sms() * 8)));
+        1, std::min<int64_t>(want, (int64_t)ep_host::grid_cap(8))));
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -1211,7 +1214,7 @@ static int launch_scatter_t(ScatterParams p, cudaStream_t stream, bool pdl) {
   }
   const int64_t work = std::max<int64_t>(p.n_units, p.n_pad_items);
   const int64_t want = (work + p.warps_per_cta - 1) / p.warps_per_cta;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::num_sms()));
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::grid_cap(1)));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(p.warps_per_cta * kWarp);
@@ -1355,7 +1358,7 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
   uint8_t* scale_rows = fp8 ? ep::scale_staging(workspace, R, T_r, k, E) : nullptr;
 
   // decode-size batches: one fused launch (layout + scatter + scales)
-  const int grid = ep_host::num_sms();
+  const int grid = ep_host::grid_cap(1);   // one CTA per SM, all resident
   if (ep_host::aligned16(topk_idx) && (int64_t)R * T_r * k < INT32_MAX) {
     ep::FusedParams fp{};
     fp.x = static_cast<const uint8_t*>(x);

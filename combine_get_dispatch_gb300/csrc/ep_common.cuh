@@ -284,7 +284,11 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 
 // Host-side helpers shared by the entry points (defined in api.cu).
 namespace ep_host {
-int num_sms();
+int num_sms();   // SMs of the current device
+// Upper bound on a data kernel's grid: ctas_per_sm CTAs on every SM, or,
+// while an SM budget is set (ep_set_num_sms), one CTA on each of that many.
+int grid_cap(int ctas_per_sm);
+bool sm_budget_set();
 void count_launch(int n = 1);
 int check_launch();   // EP_OK or EP_ERR_CUDA after a launch
 // Opt a kernel into `bytes` of dynamic shared memory on the current device

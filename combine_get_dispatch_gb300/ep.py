@@ -35,7 +35,7 @@ EXPORTS = (
     "ep_workspace_size", "ep_get_dispatch_layout", "ep_notify_dispatch", "ep_dispatch",
     "ep_combine", "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_status",
     "ep_host_wait_counters", "ep_launch_count", "ep_error_string", "ep_rank_ids",
-    "ep_rank_recv_topk", "ep_rank_combine",
+    "ep_rank_recv_topk", "ep_rank_combine", "ep_set_num_sms", "ep_get_num_sms",
 )
 
 
@@ -79,6 +79,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.ep_rank_combine.argtypes = [_P, _P, _I, _I, _I, _I, _I64, _P, _P, _P]
     L.ep_read_status.argtypes = [_P, _P, _P]
     L.ep_host_wait_counters.argtypes = [_P, _I, _I]
+    L.ep_set_num_sms.argtypes = [_I]
+    L.ep_set_num_sms.restype = _I
+    L.ep_get_num_sms.argtypes = []
+    L.ep_get_num_sms.restype = _I
     L.ep_launch_count.argtypes = []
     L.ep_launch_count.restype = ctypes.c_uint64
     L.ep_error_string.argtypes = [_I]
@@ -323,6 +327,15 @@ def ep_host_wait_counters(counters: torch.Tensor, timeout_ms: int) -> int:
     if counters.is_cuda or counters.dtype != torch.int64 or not counters.is_contiguous():
         raise ValueError("counters must be a contiguous host int64 tensor")
     return int(load().ep_host_wait_counters(_ptr(counters), counters.numel(), timeout_ms))
+
+
+def ep_set_num_sms(num_sms: int) -> None:
+    """SM budget of the data kernels (0: every SM)."""
+    _check(load().ep_set_num_sms(int(num_sms)), "ep_set_num_sms")
+
+
+def ep_get_num_sms() -> int:
+    return int(load().ep_get_num_sms())
 
 
 def ep_launch_count() -> int:

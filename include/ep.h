@@ -254,6 +254,21 @@ int ep_read_status(const int32_t* status, int32_t* host_value, void* stream);
  * ep_notify_dispatch; pure host code. */
 int ep_host_wait_counters(const volatile int64_t* counters, int n, int timeout_ms);
 
+/* SM budget (Buffer.num_sms, §2.2; the per-SM bandwidth model of §4.6):
+ * caps the SMs that the data kernels of ep_dispatch, ep_ll_dispatch,
+ * ep_combine, ep_ll_combine and ep_rank_combine occupy, so the rest of the
+ * GPU stays free for work that overlaps them.  num_sms = 0 lifts the cap
+ * (every SM; the default); num_sms > 0 launches those kernels with at most
+ * min(num_sms, SM count) CTAs of one per SM.  The single-launch low-latency
+ * path then runs on that many SMs if the batch still fits them, else the
+ * multi-kernel path is taken.  The layout and notify kernels (a few
+ * microseconds, one CTA per id chunk / one CTA) are not capped.  Process-
+ * wide, read at every launch; returns EP_ERR_INVALID_ARG for num_sms < 0.
+ * ep_get_num_sms: the CTA count one-per-SM kernels get now (the SM count of
+ * the current device, or the budget). */
+int ep_set_num_sms(int num_sms);
+int ep_get_num_sms(void);
+
 /* Number of kernels this library has launched in the process. */
 uint64_t ep_launch_count(void);
 

@@ -40,6 +40,19 @@ def test_library_is_built_for_sm_103a_only():
     assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
 
 
+def test_sm_budget_setter():
+    """ep_set_num_sms: negative budgets are refused, 0 lifts the budget
+    (host-only: the budget is read at launch time)."""
+    with pytest.raises(ep.EPError):
+        ep.ep_set_num_sms(-1)
+    ep.ep_set_num_sms(3)
+    try:
+        assert 1 <= ep.ep_get_num_sms() <= 3
+    finally:
+        ep.ep_set_num_sms(0)
+    assert ep.ep_get_num_sms() >= 1
+
+
 def test_error_strings_and_launch_counter():
     for code in range(6):
         assert ep.error_string(code)
