@@ -398,3 +398,29 @@ def alloc_workspace(R: int, T_r: int, k: int, E: int, H: int, device="cuda", str
     ws = torch.empty((ep_workspace_size(R, T_r, k, E, H),), dtype=torch.uint8, device=device)
     ep_clean_ll_buffer(None, R, E, ws, stream=stream)
     return ws
+
+
+class LowLatencyBuffers:
+    """The low-latency mode's two receive buffers (DeepEP's LL buffer holds
+    the results of at most two low-latency calls at once): two sets of
+    alloc_ll outputs, each with its own workspace, handed out in turn, so
+    the received data of call i stays valid while call i+1 dispatches into
+    the other set; call i+2 reuses the first.  Allocation only: the calls
+    themselves are the ep_ll_* entry points, issued in stream order (the
+    single-launch dispatch needs every SM, so two of them must not run
+    concurrently on different streams)."""
+
+    def __init__(self, R: int, T_r: int, H: int, E: int, k: int, max_tokens_per_rank: int,
+                 fp8_mode: int, device="cuda", stream=None):
+        self.sets = []
+        for _ in range(2):
+            b = alloc_ll(R, T_r, H, E, k, max_tokens_per_rank, fp8_mode, device=device)
+            b["workspace"] = alloc_workspace(R, T_r, k, E, H, device=device, stream=stream)
+            self.sets.append(b)
+        self._turn = 0
+
+    def next(self) -> dict:
+        """The set for the next call (alternates 0, 1, 0, ...)."""
+        b = self.sets[self._turn]
+        self._turn ^= 1
+        return b
