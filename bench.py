@@ -184,6 +184,8 @@ class Runner:
         self.rows = int((idx >= 0).sum())
         self.ll = w.mode == "ll"
         self.with_combine = with_combine
+        # a step without a host wait can be captured in a CUDA graph
+        self.capturable = self.ll or w.num_worst_tokens >= 0
         if self.ll:
             self.buf = ep.alloc_ll(w.R, w.T_r, w.H, w.E, w.k, w.max_tokens_per_rank, w.fp8_mode,
                                    device=device)
@@ -304,6 +306,56 @@ def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
     if e2e:
         res["e2e"] = measure_e2e(runner, steps, world, flush)
     return res
+
+
+def measure_launch_latency(runner, steps, flush):
+    """Launch-inclusive latency of one step (host call to completion, after
+    a synchronize on both sides): eager through the API, and the same step
+    captured once in a CUDA graph and replayed; plus the replay's device time
+    (CUDA events).  None for steps that wait on the host (normal mode without
+    num_worst_tokens cannot be captured)."""
+    import torch
+
+    if not runner.capturable:
+        return None
+
+    def wall(fn):
+        lat = []
+        for s in range(steps):
+            flush.fill_(s & 0xFF)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            lat.append((time.perf_counter() - t0) * 1e6)
+        return statistics.median(lat)
+
+    eager = wall(runner.step)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        runner.step()              # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        runner.step()
+    graph = wall(g.replay)
+    dev = []
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        dev.append(e0.elapsed_time(e1) * 1e3)
+    del g
+    code = runner.ep.ep_read_status(runner.status)
+    if code != runner.ep.EP_OK:
+        raise RuntimeError(f"{runner.w.name}: kernel status {runner.ep.error_string(code)}")
+    return {"eager_us": round(eager, 1), "graph_us": round(graph, 1),
+            "graph_device_us": round(statistics.median(dev), 1)}
 
 
 def measure_e2e(runner, steps, world, flush):
@@ -533,6 +585,8 @@ def run_ours(args, rank, world, local_rank):
         res["dispatch_gbs"] = dbytes / (res["dispatch_ms"] * 1e-3) / 1e9
         res["combine_gbs"] = cbytes / (res["combine_ms"] * 1e-3) / 1e9
         res["tokens"] = w.T
+        if name == head or name == "skewed":
+            res["launch_latency_us"] = measure_launch_latency(runner, args.steps, flush)
         results[name] = (w, runner, res)
         if name != head:
             del runner
@@ -551,7 +605,7 @@ def run_ours(args, rank, world, local_rank):
     dom = "combine" if res["combine_ms"] >= res["dispatch_ms"] else "dispatch"
     if args.no_combine:
         dom = "dispatch"
-    kern = {"combine": "k_combine", "dispatch": "k_scatter"}[dom]
+    kern = {"combine": "k_combine", "dispatch": "k_ll_fused" if runner.ll else "k_scatter"}[dom]
     src = os.path.join(ROOT, "combine_get_dispatch_gb300", "csrc",
                        "combine.cu" if dom == "combine" else "dispatch.cu")
     achieved = res[f"{dom}_gbs"]
@@ -588,9 +642,13 @@ def run_ours(args, rank, world, local_rank):
             "combine_frac": round(r["combine_gbs"] / peak, 4),
             "layout_notify_ms": round(r["step_ms"] - r["dispatch_ms"] - r["combine_ms"], 4),
             "gpu_launches": r["launches"]}
+        if r.get("launch_latency_us"):
+            others[name]["launch_latency_us"] = r["launch_latency_us"]
     line["workloads"] = others
     line["kernels_ms"] = {"dispatch": round(res["dispatch_ms"], 5),
                           "combine": round(res["combine_ms"], 5)}
+    if res.get("launch_latency_us"):
+        line["launch_latency_us"] = res["launch_latency_us"]
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
