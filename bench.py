@@ -300,7 +300,14 @@ def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
     torch.cuda.synchronize()
     disp_ms = [e[0].elapsed_time(e[1]) for e in evs]
     comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    def stats_us(v):
+        q = sorted(v)
+        return {"median": round(statistics.median(q) * 1e3, 2), "min": round(q[0] * 1e3, 2),
+                "p90": round(q[min(len(q) - 1, int(0.9 * len(q)))] * 1e3, 2)}
+
     res = {"step_ms": statistics.mean(step_ms), "step_ms_min": min(step_ms),
+           "step_us_stats": stats_us(step_ms), "dispatch_us_stats": stats_us(disp_ms),
+           "combine_us_stats": stats_us(comb_ms),
            "dispatch_ms": statistics.mean(disp_ms), "combine_ms": statistics.mean(comb_ms),
            "launches": launches, "wall_s": wall}
     if e2e:
@@ -644,11 +651,15 @@ def run_ours(args, rank, world, local_rank):
             "gpu_launches": r["launches"]}
         if r.get("launch_latency_us"):
             others[name]["launch_latency_us"] = r["launch_latency_us"]
+        for key in ("step_us_stats", "dispatch_us_stats", "combine_us_stats"):
+            others[name][key] = r[key]
     line["workloads"] = others
     line["kernels_ms"] = {"dispatch": round(res["dispatch_ms"], 5),
                           "combine": round(res["combine_ms"], 5)}
     if res.get("launch_latency_us"):
         line["launch_latency_us"] = res["launch_latency_us"]
+    for key in ("step_us_stats", "dispatch_us_stats", "combine_us_stats"):
+        line[key] = res[key]
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
