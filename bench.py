@@ -37,6 +37,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 HEADLINE = "decode"
+# bench-only workloads: a base workload run through another layout
+# ("rank": the once-per-rank receive layout of V1's normal mode)
+DERIVED = {"prefill_v1": ("prefill", {"mode": "rank"})}
+
+
+def workload(name: str):
+    from combine_get_dispatch_gb300 import synth
+    if name in DERIVED:
+        base, changes = DERIVED[name]
+        return synth.scaled(synth.WORKLOADS[base], name=name, **changes)
+    return synth.WORKLOADS[name]
 FLUSH_BYTES = 512 << 20
 
 
@@ -46,7 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workloads", default="decode,prefill,skewed,large")
+    ap.add_argument("--workloads", default="decode,prefill,skewed,large,prefill_v1")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     # profiling aids (change the workload; never used for a reported number)
@@ -183,6 +194,7 @@ class Runner:
         self.out = torch.empty_like(self.x)
         self.rows = int((idx >= 0).sum())
         self.ll = w.mode == "ll"
+        self.rank = w.mode == "rank"
         self.with_combine = with_combine
         # a step without a host wait can be captured in a CUDA graph
         self.capturable = self.ll or w.num_worst_tokens >= 0
@@ -192,6 +204,22 @@ class Runner:
             S = w.R * w.max_tokens_per_rank
             if with_combine:
                 self.y = synth.expert_outputs_torch(w.E * S, w.H, device).view(w.R, w.E_l, S, w.H)
+        elif self.rank:   # once per (token, destination rank): experts' = ranks
+            E_l = w.E // w.R
+            r_of = np.where(idx >= 0, idx // E_l, -1)
+            self.rows = int(sum(len(set(v[v >= 0].tolist())) for v in r_of.reshape(-1, w.k)))
+            self.rank_ids = torch.empty_like(self.idx)
+            self.lay = ep.alloc_layout(w.R, w.T_r, w.k, w.R, device=device)
+            self.nt = ep.alloc_notify(w.R, w.R, device=device)
+            self.host_rows = torch.empty(w.R, dtype=torch.int64).pin_memory()
+            self._layout_notify()
+            self.cap = int(self.host_rows.max())
+            self.buf = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, self.cap, device=device)
+            self.rtk = torch.empty((w.R, self.cap, w.k), dtype=torch.int64, device=device)
+            self.rtw = torch.empty((w.R, self.cap, w.k), dtype=torch.float32, device=device)
+            if with_combine:
+                self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(
+                    w.R, self.cap, w.H)
         else:
             self.lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E, device=device)
             self.nt = ep.alloc_notify(w.R, w.E, device=device)
@@ -209,6 +237,17 @@ class Runner:
 
     def _layout_notify(self):
         ep, w = self.ep, self.w
+        if self.rank:
+            ep.ep_rank_ids(self.idx, w.E, self.rank_ids, self.status)
+            ep.ep_get_dispatch_layout(self.rank_ids, w.R, self.lay["num_tokens_per_rank"],
+                                      self.lay["num_tokens_per_expert"],
+                                      self.lay["is_token_in_rank"], self.lay["slot_rank"], self.ws,
+                                      self.status)
+            ep.ep_notify_dispatch(self.lay["num_tokens_per_rank"], self.lay["num_tokens_per_expert"],
+                                  1, -1, self.nt["rank_prefix_matrix"], self.nt["expert_prefix"],
+                                  self.nt["num_recv_tokens_per_expert"], self.nt["psum"],
+                                  self.host_rows, 10000, self.status)
+            return
         ep.ep_get_dispatch_layout(self.idx, w.E, self.lay["num_tokens_per_rank"],
                                   self.lay["num_tokens_per_expert"], self.lay["is_token_in_rank"],
                                   self.lay["slot_rank"], self.ws, self.status)
@@ -237,6 +276,23 @@ class Runner:
                                  self.out, self.status)
             if ev:
                 ev[3].record()
+        elif self.rank:
+            self._layout_notify()
+            if ev:
+                ev[0].record()
+            ep.ep_dispatch(self.x, self.rank_ids, self.lay["slot_rank"], self.nt["expert_prefix"],
+                           self.nt["psum"], w.R, w.fp8_mode, self.cap, b["recv_x"],
+                           b["recv_scales"], b["recv_src_idx"], b["combine_idx"], self.ws,
+                           self.status)
+            ep.ep_rank_recv_topk(self.idx, self.wts, b["combine_idx"], w.E, self.cap, self.rtk,
+                                 self.rtw, self.status)
+            if ev:
+                ev[1].record()
+                ev[2].record()
+            if self.with_combine:
+                ep.ep_rank_combine(self.y, b["combine_idx"], self.cap, self.out, self.status)
+            if ev:
+                ev[3].record()
         else:
             self._layout_notify()
             if ev:
@@ -256,7 +312,8 @@ class Runner:
 
 def workload_desc(w) -> str:
     fp8 = {0: "bf16", 1: "FP8 E4M3 + fp32 per-128 scales", 2: "FP8 E4M3 + ue8m0 per-128 scales"}
-    mode = "low-latency packed" if w.mode == "ll" else "normal contiguous"
+    mode = {"ll": "low-latency packed", "rank": "once-per-rank (V1) normal"}.get(
+        w.mode, "normal contiguous")
     extra = f", num_worst_tokens={w.num_worst_tokens}" if w.num_worst_tokens >= 0 else ""
     return (f"{w.name}: R={w.R} x {w.T_r} tokens/rank, H={w.H}, E={w.E} ({w.E_l}/rank), "
             f"top-{w.k}, {fp8[w.fp8_mode]} {mode} dispatch + bf16 combine{extra}")
@@ -530,7 +587,7 @@ def run_sm_sweep(args, local_rank):
     budgets = [int(b) for b in args.sm_sweep.split(",") if b.strip()]
     try:
         for name in [n.strip() for n in args.workloads.split(",") if n.strip()]:
-            w = synth.WORKLOADS[name]
+            w = workload(name)
             runner = Runner(w, dev)
             row_in = 2 * w.H
             row_out = (2 * w.H if w.fp8_mode == 0
@@ -572,7 +629,7 @@ def run_ours(args, rank, world, local_rank):
     results = {}
     clocks = None
     for name in names:
-        w = synth.WORKLOADS[name]
+        w = workload(name)
         if args.tokens_per_rank > 0:
             w = synth.scaled(w, T_r=args.tokens_per_rank,
                              max_tokens_per_rank=max(w.max_tokens_per_rank, args.tokens_per_rank),
