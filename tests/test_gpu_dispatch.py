@@ -210,3 +210,25 @@ def test_fixed_shape_normal_path_replays_as_a_cuda_graph(fp8_mode):
         assert np.array_equal(got_x[rows], ref["recv_x"].reshape(w.R * cap, -1)[rows])
         want = oracle.combine(y_rows, wts, ref["combine_idx"], w.H)["out"]
         assert np.array_equal(np_(out).reshape(want.shape), want)
+
+
+@pytest.mark.parametrize("fp8_mode", [0, 2])
+def test_handle_reuse_across_dispatches(fp8_mode):
+    """The layout and notify outputs are the dispatch handle (§2.3, §4.3):
+    computed once for a routing, they serve any number of dispatches of new
+    activations with that routing, with no layout or notify in between
+    (each dispatch bit-exact vs the oracle)."""
+    w = synth.scaled(synth.WORKLOADS["prefill"], T_r=48, fp8_mode=fp8_mode)
+    _, _, idx_dev, idx, _, _ = inputs(w, seed=2)
+    lay = gpu_layout(idx_dev, w.E)
+    nt = gpu_notify(lay, w.E, 1, -1)
+    torch.cuda.synchronize()
+    cap = max(1, int(np_(nt["psum"])[:, -1].max()))
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    for seed in (3, 4, 5):
+        x_host = synth.activations(w, seed=seed)
+        x_dev = to_dev_bf16(x_host)
+        d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, fp8_mode, cap, ws=ws)
+        torch.cuda.synchronize()
+        assert ep.ep_read_status(d["status"]) == ep.EP_OK
+        _compare_full(w, x_host, idx, d, cap, 1)
