@@ -36,6 +36,7 @@ EXPORTS = (
     "ep_combine", "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_status",
     "ep_host_wait_counters", "ep_launch_count", "ep_error_string", "ep_rank_ids",
     "ep_rank_recv_topk", "ep_rank_combine", "ep_set_num_sms", "ep_get_num_sms",
+    "ep_format_e4m3", "ep_format_bf16",
 )
 
 
@@ -79,6 +80,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.ep_rank_combine.argtypes = [_P, _P, _I, _I, _I, _I, _I64, _P, _P, _P]
     L.ep_read_status.argtypes = [_P, _P, _P]
     L.ep_host_wait_counters.argtypes = [_P, _I, _I]
+    L.ep_format_e4m3.argtypes = [_P, _P, _I64, _P]
+    L.ep_format_e4m3.restype = _I
+    L.ep_format_bf16.argtypes = [_P, _P, _I64, _P]
+    L.ep_format_bf16.restype = _I
     L.ep_set_num_sms.argtypes = [_I]
     L.ep_set_num_sms.restype = _I
     L.ep_get_num_sms.argtypes = []
@@ -327,6 +332,22 @@ def ep_host_wait_counters(counters: torch.Tensor, timeout_ms: int) -> int:
     if counters.is_cuda or counters.dtype != torch.int64 or not counters.is_contiguous():
         raise ValueError("counters must be a contiguous host int64 tensor")
     return int(load().ep_host_wait_counters(_ptr(counters), counters.numel(), timeout_ms))
+
+
+def ep_format_e4m3(x, out, stream=None):
+    """fp32 -> E4M3 bytes as the FP8 dispatch casts (x float32, out uint8)."""
+    _need(x, torch.float32, name="x")
+    _need(out, torch.uint8, tuple(x.shape), "out")
+    _check(load().ep_format_e4m3(_ptr(x), _ptr(out), x.numel(), _stream(stream)), "ep_format_e4m3")
+
+
+def ep_format_bf16(x, out, stream=None):
+    """fp32 -> bf16 as the combine rounds (x float32, out bfloat16 or int16)."""
+    _need(x, torch.float32, name="x")
+    if out.dtype not in (torch.bfloat16, torch.int16):
+        raise ValueError("out must be bfloat16 or int16")
+    _need(out, None, tuple(x.shape), "out")
+    _check(load().ep_format_bf16(_ptr(x), _ptr(out), x.numel(), _stream(stream)), "ep_format_bf16")
 
 
 def ep_set_num_sms(num_sms: int) -> None:

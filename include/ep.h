@@ -254,6 +254,16 @@ int ep_read_status(const int32_t* status, int32_t* host_value, void* stream);
  * ep_notify_dispatch; pure host code. */
 int ep_host_wait_counters(const volatile int64_t* counters, int n, int timeout_ms);
 
+/* Number formats, as the kernels convert (elementwise over n floats, n
+ * even; in 8-byte and out 4-byte aligned device memory):
+ *   ep_format_e4m3: fp32 -> OCP E4M3 byte, round to nearest even, finite
+ *     values saturate to +-448 (the FP8 dispatch's cast, §1.1, §1.2);
+ *   ep_format_bf16: fp32 -> bfloat16 bits, round to nearest even (the
+ *     combine's output rounding).
+ * EP_ERR_INVALID_ARG for odd n, null or misaligned pointers. */
+int ep_format_e4m3(const float* in, uint8_t* out, int64_t n, void* stream);
+int ep_format_bf16(const float* in, uint16_t* out, int64_t n, void* stream);
+
 /* SM budget (Buffer.num_sms, §2.2; the per-SM bandwidth model of §4.6):
  * caps the SMs that the data kernels of ep_dispatch, ep_ll_dispatch,
  * ep_combine, ep_ll_combine and ep_rank_combine occupy, so the rest of the
