@@ -65,6 +65,9 @@ def parse_args(argv=None):
                     help="override T_r of every selected workload (profiling only)")
     ap.add_argument("--no-combine", action="store_true",
                     help="dispatch only, no expert-output buffer (profiling only)")
+    ap.add_argument("--separate-layout-notify", action="store_true",
+                    help="normal mode: ep_get_dispatch_layout + ep_notify_dispatch as two "
+                         "launches instead of ep_layout_notify (comparison)")
     ap.add_argument("--sm-sweep", default="",
                     help="comma list of SM budgets (ep_set_num_sms): print one line per "
                          "workload and budget with GB/s per SM instead of the headline line")
@@ -179,12 +182,13 @@ def alg_bytes(w, rows: int):
 class Runner:
     """Buffers and one step of one workload on the current GPU."""
 
-    def __init__(self, w, device, with_combine=True):
+    def __init__(self, w, device, with_combine=True, fused_layout_notify=True):
         import numpy as np
         import torch
 
         from combine_get_dispatch_gb300 import ep, synth
         self.w, self.dev, self.ep = w, device, ep
+        self.fused_layout_notify = fused_layout_notify
         idx, wts = synth.routing(w)
         self.idx = torch.from_numpy(idx).to(device)
         self.wts = torch.from_numpy(wts).to(device)
@@ -237,25 +241,21 @@ class Runner:
 
     def _layout_notify(self):
         ep, w = self.ep, self.w
-        if self.rank:
+        ids, E, A, nwt = self.idx, w.E, w.expert_alignment, w.num_worst_tokens
+        if self.rank:   # experts' = ranks, over the per-slot destination ranks
             ep.ep_rank_ids(self.idx, w.E, self.rank_ids, self.status)
-            ep.ep_get_dispatch_layout(self.rank_ids, w.R, self.lay["num_tokens_per_rank"],
-                                      self.lay["num_tokens_per_expert"],
-                                      self.lay["is_token_in_rank"], self.lay["slot_rank"], self.ws,
-                                      self.status)
-            ep.ep_notify_dispatch(self.lay["num_tokens_per_rank"], self.lay["num_tokens_per_expert"],
-                                  1, -1, self.nt["rank_prefix_matrix"], self.nt["expert_prefix"],
-                                  self.nt["num_recv_tokens_per_expert"], self.nt["psum"],
-                                  self.host_rows, 10000, self.status)
+            ids, E, A, nwt = self.rank_ids, w.R, 1, -1
+        host = self.host_rows if nwt < 0 else None
+        if self.fused_layout_notify:   # one launch (ep_layout_notify)
+            ep.ep_layout_notify(ids, E, A, nwt, self.lay, self.nt, self.ws, host, 10000,
+                                self.status)
             return
-        ep.ep_get_dispatch_layout(self.idx, w.E, self.lay["num_tokens_per_rank"],
+        ep.ep_get_dispatch_layout(ids, E, self.lay["num_tokens_per_rank"],
                                   self.lay["num_tokens_per_expert"], self.lay["is_token_in_rank"],
                                   self.lay["slot_rank"], self.ws, self.status)
         ep.ep_notify_dispatch(self.lay["num_tokens_per_rank"], self.lay["num_tokens_per_expert"],
-                              w.expert_alignment, w.num_worst_tokens,
-                              self.nt["rank_prefix_matrix"], self.nt["expert_prefix"],
-                              self.nt["num_recv_tokens_per_expert"], self.nt["psum"],
-                              self.host_rows if w.num_worst_tokens < 0 else None, 10000,
+                              A, nwt, self.nt["rank_prefix_matrix"], self.nt["expert_prefix"],
+                              self.nt["num_recv_tokens_per_expert"], self.nt["psum"], host, 10000,
                               self.status)
 
     def step(self, ev=None):
@@ -635,7 +635,8 @@ def run_ours(args, rank, world, local_rank):
                              max_tokens_per_rank=max(w.max_tokens_per_rank, args.tokens_per_rank),
                              num_worst_tokens=(w.R * args.tokens_per_rank
                                                if w.num_worst_tokens >= 0 else -1))
-        runner = Runner(w, dev, with_combine=not args.no_combine)
+        runner = Runner(w, dev, with_combine=not args.no_combine,
+                        fused_layout_notify=not args.separate_layout_notify)
         sampler = ClockSampler(local_rank) if name == head else None
         if sampler:
             sampler.start()

@@ -289,15 +289,26 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
   }
 
   // ---- the last CTA to finish resets the ticket state for the next launch
+  //      (and, layout and notify fused, computes the notify tables: every
+  //      other CTA's count rows are out before its arrival)
+  __shared__ int s_last;
   __syncthreads();
   if (tid == 0) {
+    if (p.fuse_notify) __threadfence();   // this CTA's count rows, before the arrival
     const uint32_t d = atomicAdd(&p.ctl[1], 1u);
-    if (d == (uint32_t)p.num_chunks - 1) {
+    const bool last = d == (uint32_t)p.num_chunks - 1;
+    if (last) {
       p.ctl[0] = 0;
       p.ctl[1] = 0;
       p.ctl[2] = s_epoch + 1;
       p.ctl[3] = 0;
+      if (p.fuse_notify) __threadfence();   // ... and everyone else's, before the reads
     }
+    s_last = last;
+  }
+  if (!kLL && p.fuse_notify) {
+    __syncthreads();
+    if (s_last) notify_tables<true>(p.nt, tid, kLayoutThreads, smem);   // smem is free now
   }
 }
 
@@ -358,6 +369,65 @@ int launch_layout(const LayoutParams& p, bool ll, void* ws, cudaStream_t stream)
 }
 
 }  // namespace ep
+
+extern "C" int ep_layout_notify(const int64_t* topk_idx, int R, int T_r, int k, int E,
+                                int expert_alignment, int64_t num_worst_tokens,
+                                int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                                uint8_t* is_token_in_rank, int32_t* slot_rank,
+                                int32_t* rank_prefix_matrix, int32_t* expert_prefix,
+                                int32_t* num_recv_tokens_per_expert, int64_t* psum,
+                                int64_t* host_recv_rows, int timeout_ms, void* workspace,
+                                size_t workspace_bytes, int32_t* status, void* stream) {
+  if (R <= 0 || R > ep::kMaxR || E <= 0 || E > ep::kMaxE || E % R != 0 || k <= 0 ||
+      k > ep::kMaxK || T_r < 0 || expert_alignment <= 0)
+    return EP_ERR_INVALID_ARG;
+  if (!num_tokens_per_rank || !num_tokens_per_expert || !workspace || !rank_prefix_matrix ||
+      !expert_prefix || !num_recv_tokens_per_expert || !psum ||
+      (T_r > 0 && (!topk_idx || !is_token_in_rank || !slot_rank)))
+    return EP_ERR_INVALID_ARG;
+  if (workspace_bytes < ep::layout_geometry(R, T_r, k, E, ep::kNormalChunkIds).bytes)
+    return EP_ERR_INVALID_ARG;
+  ep::LayoutParams p{};
+  p.topk_idx = topk_idx;
+  p.R = R;
+  p.T_r = T_r;
+  p.k = k;
+  p.E = E;
+  p.E_l = E / R;
+  p.num_tokens_per_rank = num_tokens_per_rank;
+  p.num_tokens_per_expert = num_tokens_per_expert;
+  p.is_token_in_rank = is_token_in_rank;
+  p.slot_rank = slot_rank;
+  p.status = status;
+  p.fuse_notify = true;
+  ep::NotifyParams& n = p.nt;
+  n.num_tokens_per_rank = num_tokens_per_rank;
+  n.num_tokens_per_expert = num_tokens_per_expert;
+  n.R = R;
+  n.E = E;
+  n.E_l = E / R;
+  n.expert_alignment = expert_alignment;
+  n.num_worst_tokens = num_worst_tokens;
+  n.rank_prefix_matrix = rank_prefix_matrix;
+  n.expert_prefix = expert_prefix;
+  n.num_recv_tokens_per_expert = num_recv_tokens_per_expert;
+  n.psum = psum;
+  n.status = status;
+  const bool wait = host_recv_rows != nullptr && num_worst_tokens < 0;
+  if (host_recv_rows != nullptr) {
+    void* dev = nullptr;
+    if (cudaHostGetDevicePointer(&dev, host_recv_rows, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return EP_ERR_INVALID_ARG;
+    }
+    volatile int64_t* h = host_recv_rows;
+    for (int r = 0; r < R; ++r) h[r] = -1;
+    n.host_recv_rows = static_cast<int64_t*>(dev);
+  }
+  const int rc = ep::launch_layout(p, false, workspace, static_cast<cudaStream_t>(stream));
+  if (rc != EP_OK || !wait) return rc;
+  return ep_host_wait_counters(host_recv_rows, R, timeout_ms);
+}
 
 extern "C" int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E,
                                       int32_t* num_tokens_per_rank,

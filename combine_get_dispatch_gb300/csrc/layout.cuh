@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "notify.cuh"
+
 namespace ep {
 
 struct LayoutParams {
@@ -27,6 +29,10 @@ struct LayoutParams {
   uint64_t* flags;      // [num_chunks][V] look-back words
   uint64_t* rank_start;  // [R][E] low-latency: tagged prefix at the start of each rank
   int32_t* status;
+  // normal mode, layout and notify in one launch: the last CTA to finish
+  // computes the notify tables from the count tables the CTAs wrote
+  bool fuse_notify;
+  NotifyParams nt;
 };
 
 struct LayoutGeometry {

@@ -36,7 +36,7 @@ EXPORTS = (
     "ep_combine", "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_status",
     "ep_host_wait_counters", "ep_launch_count", "ep_error_string", "ep_rank_ids",
     "ep_rank_recv_topk", "ep_rank_combine", "ep_set_num_sms", "ep_get_num_sms",
-    "ep_format_e4m3", "ep_format_bf16",
+    "ep_format_e4m3", "ep_format_bf16", "ep_layout_notify",
 )
 
 
@@ -80,6 +80,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.ep_rank_combine.argtypes = [_P, _P, _I, _I, _I, _I, _I64, _P, _P, _P]
     L.ep_read_status.argtypes = [_P, _P, _P]
     L.ep_host_wait_counters.argtypes = [_P, _I, _I]
+    L.ep_layout_notify.argtypes = [_P, _I, _I, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, _I, _P, _SZ, _P, _P]
+    L.ep_layout_notify.restype = _I
     L.ep_format_e4m3.argtypes = [_P, _P, _I64, _P]
     L.ep_format_e4m3.restype = _I
     L.ep_format_bf16.argtypes = [_P, _P, _I64, _P]
@@ -184,6 +187,38 @@ def ep_notify_dispatch(num_tokens_per_rank, num_tokens_per_expert, expert_alignm
                                    _ptr(psum), _ptr(host_recv_rows), timeout_ms, _ptr(status),
                                    _stream(stream))
     _check(rc, "ep_notify_dispatch")
+
+
+def ep_layout_notify(topk_idx, num_experts, expert_alignment, num_worst_tokens, lay, nt,
+                     workspace, host_recv_rows=None, timeout_ms=10000, status=None, stream=None):
+    """ep_get_dispatch_layout + ep_notify_dispatch in one launch; `lay` and
+    `nt` are the dicts of alloc_layout / alloc_notify."""
+    R, T_r, k = topk_idx.shape
+    E = num_experts
+    E_l = E // R
+    _need(topk_idx, torch.int64, name="topk_idx")
+    _need(lay["num_tokens_per_rank"], torch.int32, (R, R), "num_tokens_per_rank")
+    _need(lay["num_tokens_per_expert"], torch.int32, (R, E), "num_tokens_per_expert")
+    _need(lay["is_token_in_rank"], torch.uint8, (R, T_r, R), "is_token_in_rank")
+    _need(lay["slot_rank"], torch.int32, (R, T_r, k), "slot_rank")
+    _need(nt["rank_prefix_matrix"], torch.int32, (R, R), "rank_prefix_matrix")
+    _need(nt["expert_prefix"], torch.int32, (R + 1, E), "expert_prefix")
+    _need(nt["num_recv_tokens_per_expert"], torch.int32, (R, E_l), "num_recv_tokens_per_expert")
+    _need(nt["psum"], torch.int64, (R, E_l + 1), "psum")
+    _need(workspace, torch.uint8, name="workspace")
+    _need(status, torch.int32, (1,), "status", optional=True)
+    if host_recv_rows is not None:
+        if host_recv_rows.is_cuda or not host_recv_rows.is_pinned() or \
+                host_recv_rows.dtype != torch.int64 or host_recv_rows.numel() < R:
+            raise ValueError("host_recv_rows must be a pinned host int64 tensor of >= R entries")
+    rc = load().ep_layout_notify(_ptr(topk_idx), R, T_r, k, E, expert_alignment, num_worst_tokens,
+                                 _ptr(lay["num_tokens_per_rank"]), _ptr(lay["num_tokens_per_expert"]),
+                                 _ptr(lay["is_token_in_rank"]), _ptr(lay["slot_rank"]),
+                                 _ptr(nt["rank_prefix_matrix"]), _ptr(nt["expert_prefix"]),
+                                 _ptr(nt["num_recv_tokens_per_expert"]), _ptr(nt["psum"]),
+                                 _ptr(host_recv_rows), timeout_ms, _ptr(workspace),
+                                 workspace.numel(), _ptr(status), _stream(stream))
+    _check(rc, "ep_layout_notify")
 
 
 def ep_dispatch(x, topk_idx, slot_rank, expert_prefix, psum, num_experts, fp8_mode, cap_rows,

@@ -133,6 +133,20 @@ int ep_notify_dispatch(const int32_t* num_tokens_per_rank, const int32_t* num_to
                        int32_t* num_recv_tokens_per_expert, int64_t* psum,
                        int64_t* host_recv_rows, int timeout_ms, int32_t* status, void* stream);
 
+/* get_dispatch_layout and notify_dispatch in ONE launch (the V2 design of
+ * §4.6 folds notify into the dispatch-side grid): the layout kernel's last
+ * CTA to finish computes the notify tables from the count tables the other
+ * CTAs wrote.  Arguments, outputs, host handshake and errors are those of
+ * ep_get_dispatch_layout followed by ep_notify_dispatch on the same
+ * stream; the outputs are identical. */
+int ep_layout_notify(const int64_t* topk_idx, int R, int T_r, int k, int E, int expert_alignment,
+                     int64_t num_worst_tokens, int32_t* num_tokens_per_rank,
+                     int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                     int32_t* slot_rank, int32_t* rank_prefix_matrix, int32_t* expert_prefix,
+                     int32_t* num_recv_tokens_per_expert, int64_t* psum,
+                     int64_t* host_recv_rows, int timeout_ms, void* workspace,
+                     size_t workspace_bytes, int32_t* status, void* stream);
+
 /* Normal-mode dispatch into the contiguous per-expert layout (§1.1, §2.3,
  * §4.3).  Slot (i, t, j) with expert e = r*E_l + l is copied (or quantised)
  * into rank r's row psum[r][l] + expert_prefix[i][e] + slot_rank[i][t][j].
