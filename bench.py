@@ -258,6 +258,16 @@ class Runner:
                               self.nt["num_recv_tokens_per_expert"], self.nt["psum"], host, 10000,
                               self.status)
 
+    def step_single_call(self):
+        """Fixed-shape normal mode: ep_layout_notify_dispatch (layout + notify,
+        then the dispatch as its programmatic dependent), then the combine."""
+        ep, w, b = self.ep, self.w, self.buf
+        ep.ep_layout_notify_dispatch(self.x, self.idx, w.E, w.fp8_mode, w.expert_alignment,
+                                     w.num_worst_tokens, self.cap, self.lay, self.nt, b, self.ws,
+                                     self.status)
+        if self.with_combine:
+            ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
+
     def step(self, ev=None):
         """One pass; ev = (e0, e1, e2, e3) events around dispatch / combine."""
         ep, w, b = self.ep, self.w, self.buf
@@ -370,6 +380,37 @@ def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
     if e2e:
         res["e2e"] = measure_e2e(runner, steps, world, flush)
     return res
+
+
+def measure_single_call(runner, steps, flush):
+    """The fixed-shape normal step through ep_layout_notify_dispatch: device
+    time per step (events around it, L2 flushed before each) and its
+    launch-inclusive latency, eager and replayed as a CUDA graph."""
+    import torch
+
+    for _ in range(3):
+        flush.fill_(1)
+        runner.step_single_call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        ev[s][0].record()
+        runner.step_single_call()
+        ev[s][1].record()
+    torch.cuda.synchronize()
+    code = runner.ep.ep_read_status(runner.status)
+    if code != runner.ep.EP_OK:
+        raise RuntimeError(f"{runner.w.name}: kernel status {runner.ep.error_string(code)}")
+    out = {"step_us": round(statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3, 2)}
+    step = runner.step
+    runner.step = runner.step_single_call    # the latency helper captures runner.step
+    try:
+        out.update(measure_launch_latency(runner, steps, flush) or {})
+    finally:
+        runner.step = step
+    return out
 
 
 def measure_launch_latency(runner, steps, flush):
@@ -652,6 +693,8 @@ def run_ours(args, rank, world, local_rank):
         res["tokens"] = w.T
         if name == head or name == "skewed":
             res["launch_latency_us"] = measure_launch_latency(runner, args.steps, flush)
+        if not runner.ll and not runner.rank and w.num_worst_tokens >= 0 and not args.no_combine:
+            res["single_call"] = measure_single_call(runner, args.steps, flush)
         results[name] = (w, runner, res)
         if name != head:
             del runner
@@ -709,6 +752,8 @@ def run_ours(args, rank, world, local_rank):
             "gpu_launches": r["launches"]}
         if r.get("launch_latency_us"):
             others[name]["launch_latency_us"] = r["launch_latency_us"]
+        if r.get("single_call"):
+            others[name]["single_call"] = r["single_call"]
         for key in ("step_us_stats", "dispatch_us_stats", "combine_us_stats"):
             others[name][key] = r[key]
     line["workloads"] = others
@@ -716,6 +761,8 @@ def run_ours(args, rank, world, local_rank):
                           "combine": round(res["combine_ms"], 5)}
     if res.get("launch_latency_us"):
         line["launch_latency_us"] = res["launch_latency_us"]
+    if res.get("single_call"):
+        line["single_call"] = res["single_call"]
     for key in ("step_us_stats", "dispatch_us_stats", "combine_us_stats"):
         line[key] = res[key]
     if rank == 0:

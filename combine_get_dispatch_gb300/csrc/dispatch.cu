@@ -436,6 +436,10 @@ __global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterPar
     pipe_run<kMode>(q, PackedDest{&p}, lane, ld);
     return;
   }
+  // launched as a programmatic dependent of the layout + notify kernel, the
+  // first x pieces went out above; the prefix tables are read from here on
+  // (a no-op after an ordinary launch)
+  pdl_wait();
   pipe_run<kMode>(q, NormalDest{&p}, lane, ld);
   pad_fill(p, gw, W, lane);
 }
@@ -1016,6 +1020,9 @@ struct ScaleColParams {
   const int64_t* psum;         // normal mode: [R][E_l + 1] segment starts
   const int32_t* expert_total; // normal mode: [E] rows of every expert (unaligned)
   int E, E_l;
+  bool tables_after_wait;      // normal mode: the segment tables may still be in the making
+                               // when this kernel starts (the scatter itself was a dependent
+                               // launch of layout + notify): read them after the wait
   void* out;                   // column-major scales [segment][block][row]
 };
 
@@ -1075,6 +1082,7 @@ __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColPara
     }
     return;
   }
+  if (p.tables_after_wait) pdl_wait();
   __shared__ int32_t s_base[kMaxE + 1];   // exclusive prefix of the valid rows per segment
   __shared__ int32_t s_start[kMaxE];      // first row of every segment in its rank
   __shared__ int32_t s_warp[kScaleColThreads / kWarp];
@@ -1116,9 +1124,10 @@ __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColPara
   }
   if (tid == kScaleColThreads - 1) s_base[p.E] = run;   // the last thread holds the total
   __syncthreads();
-  // the segment tables come from notify, complete before the scatter began;
-  // the staged scales and row sources need the scatter itself
-  pdl_wait();
+  // the segment tables come from notify, complete before the scatter began
+  // (unless tables_after_wait); the staged scales and row sources need the
+  // scatter itself
+  if (!p.tables_after_wait) pdl_wait();
   const int32_t total = s_base[p.E];
   for (int32_t f = blockIdx.x * kScaleColThreads + tid; f < total;
        f += gridDim.x * kScaleColThreads) {
@@ -1233,13 +1242,17 @@ static int launch_scatter_t(ScatterParams p, cudaStream_t stream, bool pdl) {
   return ep_host::check_launch();
 }
 
-static int launch_scatter(const ScatterParams& p, int fp8_mode, bool ll, cudaStream_t stream) {
+// Normal mode: pdl when the previous kernel on the stream is this library's
+// layout + notify kernel launched to trigger it (its x loads then overlap
+// the layout); low-latency mode always follows its layout kernel that way.
+static int launch_scatter(const ScatterParams& p, int fp8_mode, bool ll, cudaStream_t stream,
+                          bool pdl_normal = false) {
   switch (fp8_mode * 2 + (ll ? 1 : 0)) {
-    case 0: return launch_scatter_t<EP_FP8_NONE, false>(p, stream, false);
+    case 0: return launch_scatter_t<EP_FP8_NONE, false>(p, stream, pdl_normal);
     case 1: return launch_scatter_t<EP_FP8_NONE, true>(p, stream, true);
-    case 2: return launch_scatter_t<EP_FP8_E4M3_F32_SCALE, false>(p, stream, false);
+    case 2: return launch_scatter_t<EP_FP8_E4M3_F32_SCALE, false>(p, stream, pdl_normal);
     case 3: return launch_scatter_t<EP_FP8_E4M3_F32_SCALE, true>(p, stream, true);
-    case 4: return launch_scatter_t<EP_FP8_E4M3_UE8M0, false>(p, stream, false);
+    case 4: return launch_scatter_t<EP_FP8_E4M3_UE8M0, false>(p, stream, pdl_normal);
     case 5: return launch_scatter_t<EP_FP8_E4M3_UE8M0, true>(p, stream, true);
   }
   return EP_ERR_INVALID_ARG;
@@ -1271,12 +1284,12 @@ extern "C" size_t ep_workspace_size(int R, int T_r, int k, int E, int H) {
   return ep::layout_region_bytes(R, T_r, k, E) + ep::staging_bytes(R, T_r, H);
 }
 
-extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t* slot_rank,
+static int dispatch_normal(const void* x, const int64_t* topk_idx, const int32_t* slot_rank,
                            const int32_t* expert_prefix, const int64_t* psum, int R, int T_r,
                            int H, int E, int k, int fp8_mode, int64_t cap_rows, void* recv_x,
                            void* recv_scales, int32_t* recv_src_idx, int32_t* combine_idx,
                            void* workspace, size_t workspace_bytes, int32_t* status,
-                           void* stream) {
+                           void* stream, bool pdl) {
   int rc = ep::check_common(R, T_r, H, E, k, fp8_mode);
   if (rc != EP_OK) return rc;
   if (cap_rows < 0 || (int64_t)R * cap_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
@@ -1316,7 +1329,7 @@ extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t
   p.status = status;
   p.tail_chunks = (int)((cap_rows + ep::kPadChunkRows - 1) / ep::kPadChunkRows);
   p.n_pad_items = (int64_t)R * p.E_l + (int64_t)R * p.tail_chunks;
-  rc = ep::launch_scatter(p, fp8_mode, false, s);
+  rc = ep::launch_scatter(p, fp8_mode, false, s, pdl);
   if (rc != EP_OK || !fp8 || cap_rows == 0) return rc;
   ep::ScaleColParams sp{};
   sp.scale_rows = p.scale_rows;
@@ -1331,7 +1344,42 @@ extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t
   sp.E = E;
   sp.E_l = E / R;
   sp.out = recv_scales;
+  sp.tables_after_wait = pdl;
   return ep::launch_scale_columns(sp, false, fp8_mode, s);
+}
+
+extern "C" int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t* slot_rank,
+                           const int32_t* expert_prefix, const int64_t* psum, int R, int T_r,
+                           int H, int E, int k, int fp8_mode, int64_t cap_rows, void* recv_x,
+                           void* recv_scales, int32_t* recv_src_idx, int32_t* combine_idx,
+                           void* workspace, size_t workspace_bytes, int32_t* status,
+                           void* stream) {
+  return dispatch_normal(x, topk_idx, slot_rank, expert_prefix, psum, R, T_r, H, E, k, fp8_mode,
+                         cap_rows, recv_x, recv_scales, recv_src_idx, combine_idx, workspace,
+                         workspace_bytes, status, stream, false);
+}
+
+extern "C" int ep_layout_notify_dispatch(
+    const void* x, const int64_t* topk_idx, int R, int T_r, int H, int E, int k, int fp8_mode,
+    int expert_alignment, int64_t num_worst_tokens, int64_t cap_rows, int32_t* num_tokens_per_rank,
+    int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank, int32_t* slot_rank,
+    int32_t* rank_prefix_matrix, int32_t* expert_prefix, int32_t* num_recv_tokens_per_expert,
+    int64_t* psum, void* recv_x, void* recv_scales, int32_t* recv_src_idx, int32_t* combine_idx,
+    void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  // fixed shape only: the receive buffers exist before the counts do
+  if (num_worst_tokens < 0) return EP_ERR_INVALID_ARG;
+  int rc = ep::check_common(R, T_r, H, E, k, fp8_mode);
+  if (rc != EP_OK) return rc;
+  if (workspace_bytes < ep_workspace_size(R, T_r, k, E, H)) return EP_ERR_INVALID_ARG;
+  rc = ep::layout_notify(topk_idx, R, T_r, k, E, expert_alignment, num_worst_tokens,
+                         num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank, slot_rank,
+                         rank_prefix_matrix, expert_prefix, num_recv_tokens_per_expert, psum,
+                         nullptr, 0, workspace, workspace_bytes, status,
+                         static_cast<cudaStream_t>(stream), true);
+  if (rc != EP_OK) return rc;
+  return dispatch_normal(x, topk_idx, slot_rank, expert_prefix, psum, R, T_r, H, E, k, fp8_mode,
+                         cap_rows, recv_x, recv_scales, recv_src_idx, combine_idx, workspace,
+                         workspace_bytes, status, stream, true);
 }
 
 extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int T_r, int H, int E,

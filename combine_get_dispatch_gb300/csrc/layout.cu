@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
   const int warp = tid >> 5;
   const int nbits = key_bits(p.E);
 
-  if (kLL) pdl_launch_dependents();   // the scatter kernel may start loading x
+  if (kLL || p.trigger_dependents) pdl_launch_dependents();   // the scatter may start loading x
   if (tid == 0) {
     s_ticket = atomicAdd(&p.ctl[0], 1u);
     s_epoch = ld_relaxed_u32(&p.ctl[2]);
@@ -370,14 +370,13 @@ int launch_layout(const LayoutParams& p, bool ll, void* ws, cudaStream_t stream)
 
 }  // namespace ep
 
-extern "C" int ep_layout_notify(const int64_t* topk_idx, int R, int T_r, int k, int E,
-                                int expert_alignment, int64_t num_worst_tokens,
-                                int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
-                                uint8_t* is_token_in_rank, int32_t* slot_rank,
-                                int32_t* rank_prefix_matrix, int32_t* expert_prefix,
-                                int32_t* num_recv_tokens_per_expert, int64_t* psum,
-                                int64_t* host_recv_rows, int timeout_ms, void* workspace,
-                                size_t workspace_bytes, int32_t* status, void* stream) {
+int ep::layout_notify(const int64_t* topk_idx, int R, int T_r, int k, int E, int expert_alignment,
+                      int64_t num_worst_tokens, int32_t* num_tokens_per_rank,
+                      int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank, int32_t* slot_rank,
+                      int32_t* rank_prefix_matrix, int32_t* expert_prefix,
+                      int32_t* num_recv_tokens_per_expert, int64_t* psum, int64_t* host_recv_rows,
+                      int timeout_ms, void* workspace, size_t workspace_bytes, int32_t* status,
+                      cudaStream_t stream, bool trigger_dependents) {
   if (R <= 0 || R > ep::kMaxR || E <= 0 || E > ep::kMaxE || E % R != 0 || k <= 0 ||
       k > ep::kMaxK || T_r < 0 || expert_alignment <= 0)
     return EP_ERR_INVALID_ARG;
@@ -400,6 +399,7 @@ extern "C" int ep_layout_notify(const int64_t* topk_idx, int R, int T_r, int k, 
   p.slot_rank = slot_rank;
   p.status = status;
   p.fuse_notify = true;
+  p.trigger_dependents = trigger_dependents;
   ep::NotifyParams& n = p.nt;
   n.num_tokens_per_rank = num_tokens_per_rank;
   n.num_tokens_per_expert = num_tokens_per_expert;
@@ -424,9 +424,25 @@ extern "C" int ep_layout_notify(const int64_t* topk_idx, int R, int T_r, int k, 
     for (int r = 0; r < R; ++r) h[r] = -1;
     n.host_recv_rows = static_cast<int64_t*>(dev);
   }
-  const int rc = ep::launch_layout(p, false, workspace, static_cast<cudaStream_t>(stream));
+  const int rc = ep::launch_layout(p, false, workspace, stream);
   if (rc != EP_OK || !wait) return rc;
   return ep_host_wait_counters(host_recv_rows, R, timeout_ms);
+}
+
+extern "C" int ep_layout_notify(const int64_t* topk_idx, int R, int T_r, int k, int E,
+                                int expert_alignment, int64_t num_worst_tokens,
+                                int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
+                                uint8_t* is_token_in_rank, int32_t* slot_rank,
+                                int32_t* rank_prefix_matrix, int32_t* expert_prefix,
+                                int32_t* num_recv_tokens_per_expert, int64_t* psum,
+                                int64_t* host_recv_rows, int timeout_ms, void* workspace,
+                                size_t workspace_bytes, int32_t* status, void* stream) {
+  return ep::layout_notify(topk_idx, R, T_r, k, E, expert_alignment, num_worst_tokens,
+                           num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank,
+                           slot_rank, rank_prefix_matrix, expert_prefix,
+                           num_recv_tokens_per_expert, psum, host_recv_rows, timeout_ms,
+                           workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream),
+                           false);
 }
 
 extern "C" int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E,

@@ -33,6 +33,7 @@ struct LayoutParams {
   // computes the notify tables from the count tables the CTAs wrote
   bool fuse_notify;
   NotifyParams nt;
+  bool trigger_dependents;   // normal mode: a programmatic dependent scatter may launch early
 };
 
 struct LayoutGeometry {
@@ -57,5 +58,16 @@ size_t layout_region_bytes(int R, int T_r, int k, int E);
 // Launch the layout kernel on workspace `ws` (normal: per-rank scan into
 // p's normal outputs; ll: global scan into p's low-latency outputs).
 int launch_layout(const LayoutParams& p, bool ll, void* ws, cudaStream_t stream);
+
+// Layout and notify in one launch (ep_layout_notify); with
+// trigger_dependents the next kernel, launched as a programmatic dependent,
+// may start before this one ends (it must wait before reading the tables).
+int layout_notify(const int64_t* topk_idx, int R, int T_r, int k, int E, int expert_alignment,
+                  int64_t num_worst_tokens, int32_t* num_tokens_per_rank,
+                  int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank, int32_t* slot_rank,
+                  int32_t* rank_prefix_matrix, int32_t* expert_prefix,
+                  int32_t* num_recv_tokens_per_expert, int64_t* psum, int64_t* host_recv_rows,
+                  int timeout_ms, void* workspace, size_t workspace_bytes, int32_t* status,
+                  cudaStream_t stream, bool trigger_dependents);
 
 }  // namespace ep

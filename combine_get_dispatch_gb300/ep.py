@@ -36,7 +36,7 @@ EXPORTS = (
     "ep_combine", "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_status",
     "ep_host_wait_counters", "ep_launch_count", "ep_error_string", "ep_rank_ids",
     "ep_rank_recv_topk", "ep_rank_combine", "ep_set_num_sms", "ep_get_num_sms",
-    "ep_format_e4m3", "ep_format_bf16", "ep_layout_notify",
+    "ep_format_e4m3", "ep_format_bf16", "ep_layout_notify", "ep_layout_notify_dispatch",
 )
 
 
@@ -83,6 +83,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.ep_layout_notify.argtypes = [_P, _I, _I, _I, _I, _I, _I64, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _I, _P, _SZ, _P, _P]
     L.ep_layout_notify.restype = _I
+    L.ep_layout_notify_dispatch.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I64, _I64, _P, _P,
+                                            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                            _P]
+    L.ep_layout_notify_dispatch.restype = _I
     L.ep_format_e4m3.argtypes = [_P, _P, _I64, _P]
     L.ep_format_e4m3.restype = _I
     L.ep_format_bf16.argtypes = [_P, _P, _I64, _P]
@@ -219,6 +223,47 @@ def ep_layout_notify(topk_idx, num_experts, expert_alignment, num_worst_tokens, 
                                  _ptr(host_recv_rows), timeout_ms, _ptr(workspace),
                                  workspace.numel(), _ptr(status), _stream(stream))
     _check(rc, "ep_layout_notify")
+
+
+def ep_layout_notify_dispatch(x, topk_idx, num_experts, fp8_mode, expert_alignment,
+                              num_worst_tokens, cap_rows, lay, nt, d, workspace, status=None,
+                              stream=None):
+    """Fixed-shape normal mode in one call: layout + notify (one launch),
+    then the dispatch as its programmatic dependent.  `lay`, `nt`, `d` are
+    the dicts of alloc_layout / alloc_notify / alloc_dispatch."""
+    R, T_r, H = x.shape
+    k = topk_idx.shape[2]
+    E = num_experts
+    E_l = E // R
+    _need(x, torch.bfloat16, (R, T_r, H), "x")
+    _need(topk_idx, torch.int64, (R, T_r, k), "topk_idx")
+    for key, dt, shape in (("num_tokens_per_rank", torch.int32, (R, R)),
+                           ("num_tokens_per_expert", torch.int32, (R, E)),
+                           ("is_token_in_rank", torch.uint8, (R, T_r, R)),
+                           ("slot_rank", torch.int32, (R, T_r, k))):
+        _need(lay[key], dt, shape, key)
+    for key, dt, shape in (("rank_prefix_matrix", torch.int32, (R, R)),
+                           ("expert_prefix", torch.int32, (R + 1, E)),
+                           ("num_recv_tokens_per_expert", torch.int32, (R, E_l)),
+                           ("psum", torch.int64, (R, E_l + 1))):
+        _need(nt[key], dt, shape, key)
+    rdt = torch.bfloat16 if fp8_mode == EP_FP8_NONE else torch.uint8
+    _need(d["recv_x"], rdt, (R, cap_rows, H), "recv_x")
+    if fp8_mode != EP_FP8_NONE:
+        _need(d["recv_scales"], _scale_dtype(fp8_mode), (R, H // 128, cap_rows), "recv_scales")
+    _need(d["recv_src_idx"], torch.int32, (R, cap_rows), "recv_src_idx")
+    _need(d["combine_idx"], torch.int32, (R, T_r, k), "combine_idx")
+    _need(workspace, torch.uint8, name="workspace")
+    _need(status, torch.int32, (1,), "status", optional=True)
+    rc = load().ep_layout_notify_dispatch(
+        _ptr(x), _ptr(topk_idx), R, T_r, H, E, k, fp8_mode, expert_alignment, num_worst_tokens,
+        cap_rows, _ptr(lay["num_tokens_per_rank"]), _ptr(lay["num_tokens_per_expert"]),
+        _ptr(lay["is_token_in_rank"]), _ptr(lay["slot_rank"]), _ptr(nt["rank_prefix_matrix"]),
+        _ptr(nt["expert_prefix"]), _ptr(nt["num_recv_tokens_per_expert"]), _ptr(nt["psum"]),
+        _ptr(d["recv_x"]), _ptr(d["recv_scales"]) if fp8_mode != EP_FP8_NONE else None,
+        _ptr(d["recv_src_idx"]), _ptr(d["combine_idx"]), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream))
+    _check(rc, "ep_layout_notify_dispatch")
 
 
 def ep_dispatch(x, topk_idx, slot_rank, expert_prefix, psum, num_experts, fp8_mode, cap_rows,

@@ -147,6 +147,22 @@ int ep_layout_notify(const int64_t* topk_idx, int R, int T_r, int k, int E, int 
                      int64_t* host_recv_rows, int timeout_ms, void* workspace,
                      size_t workspace_bytes, int32_t* status, void* stream);
 
+/* Fixed-shape normal mode (num_worst_tokens >= 0, cap_rows given) in ONE
+ * call: ep_layout_notify, then ep_dispatch launched as its programmatic
+ * dependent (the dispatch kernel's first token loads overlap the layout;
+ * it waits for the prefix tables before placing any row).  Arguments and
+ * outputs are those of the two calls; the results are identical.
+ * EP_ERR_INVALID_ARG for num_worst_tokens < 0 (no host handshake here). */
+int ep_layout_notify_dispatch(const void* x, const int64_t* topk_idx, int R, int T_r, int H, int E,
+                              int k, int fp8_mode, int expert_alignment, int64_t num_worst_tokens,
+                              int64_t cap_rows, int32_t* num_tokens_per_rank,
+                              int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                              int32_t* slot_rank, int32_t* rank_prefix_matrix,
+                              int32_t* expert_prefix, int32_t* num_recv_tokens_per_expert,
+                              int64_t* psum, void* recv_x, void* recv_scales,
+                              int32_t* recv_src_idx, int32_t* combine_idx, void* workspace,
+                              size_t workspace_bytes, int32_t* status, void* stream);
+
 /* Normal-mode dispatch into the contiguous per-expert layout (§1.1, §2.3,
  * §4.3).  Slot (i, t, j) with expert e = r*E_l + l is copied (or quantised)
  * into rank r's row psum[r][l] + expert_prefix[i][e] + slot_rank[i][t][j].

@@ -95,3 +95,122 @@ def test_fused_repeated_calls_on_one_workspace():
         idx, _ = synth.routing(w, seed=seed)
         lay, nt, st, _ = _fused(torch.from_numpy(idx).cuda(), w.E, 1, w.num_worst_tokens, ws=ws)
         _check(idx, w.E, 1, w.num_worst_tokens, lay, nt, st)
+
+
+def _single_call(w, x_dev, idx_dev, fp8_mode, A, ws=None, status=None):
+    cap = w.cap_rows()
+    lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E)
+    nt = ep.alloc_notify(w.R, w.E)
+    d = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, fp8_mode, cap)
+    for v in list(lay.values()) + list(nt.values()) + list(d.values()):
+        poison_(v)
+    ws = ws if ws is not None else ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    st = status if status is not None else status_word()
+    ep.ep_layout_notify_dispatch(x_dev, idx_dev, w.E, fp8_mode, A, w.num_worst_tokens, cap, lay,
+                                 nt, d, ws, st)
+    torch.cuda.synchronize()
+    return lay, nt, d, st, cap
+
+
+@pytest.mark.parametrize("fp8_mode,A", [(0, 1), (1, 1), (2, 128)])
+def test_single_call_fixed_shape_matches_the_separate_calls(fp8_mode, A):
+    """ep_layout_notify_dispatch (layout + notify, then the dispatch as its
+    programmatic dependent) gives exactly the separate calls' outputs."""
+    from ep_harness import gpu_dispatch, inputs
+    w = synth.scaled(synth.WORKLOADS["skewed"], T_r=96, H=1024, fp8_mode=fp8_mode,
+                     num_worst_tokens=32 * 96)
+    x_dev, _, idx_dev, idx, _, _ = inputs(w, seed=5)
+    lay, nt, d, st, cap = _single_call(w, x_dev, idx_dev, fp8_mode, A)
+    assert ep.ep_read_status(st) == ep.EP_OK
+    lay2 = gpu_layout(idx_dev, w.E)
+    nt2 = gpu_notify(lay2, w.E, A, w.num_worst_tokens)
+    d2 = gpu_dispatch(x_dev, idx_dev, lay2, nt2, w.E, fp8_mode, cap)
+    torch.cuda.synchronize()
+    for key in LAYOUT_KEYS:
+        assert torch.equal(lay2[key], lay[key]), key
+    for key in NOTIFY_KEYS:
+        assert torch.equal(nt2[key], nt[key]), key
+    assert torch.equal(d2["combine_idx"], d["combine_idx"])
+    assert torch.equal(d2["recv_src_idx"], d["recv_src_idx"])
+    rows = torch.nonzero(d["recv_src_idx"].reshape(-1) >= 0).squeeze(1)
+    rx, rx2 = d["recv_x"].reshape(w.R * cap, -1), d2["recv_x"].reshape(w.R * cap, -1)
+    assert torch.equal(rx[rows].view(torch.uint8), rx2[rows].view(torch.uint8))
+    if fp8_mode:
+        sc = d["recv_scales"].permute(0, 2, 1).reshape(w.R * cap, -1)
+        sc2 = d2["recv_scales"].permute(0, 2, 1).reshape(w.R * cap, -1)
+        assert torch.equal(sc[rows], sc2[rows])
+    # and the oracle
+    from test_gpu_dispatch import _compare_full
+    _, x_host, _, _, _, _ = inputs(w, seed=5)
+    _compare_full(w, x_host, idx, d, cap, A)
+
+
+def test_single_call_full_size_skewed_and_repeated():
+    from ep_harness import inputs
+    from test_gpu_dispatch import _compare_full
+    w = synth.WORKLOADS["skewed"]
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    for seed in (0, 1):
+        x_dev, x_host, idx_dev, idx, _, _ = inputs(w, seed=seed)
+        lay, nt, d, st, cap = _single_call(w, x_dev, idx_dev, w.fp8_mode, 1, ws=ws)
+        assert ep.ep_read_status(st) == ep.EP_OK
+        _compare_full(w, x_host, idx, d, cap, 1)
+
+
+def test_single_call_refuses_the_host_handshake_mode():
+    w = synth.scaled(synth.WORKLOADS["prefill"], T_r=8)
+    x = torch.zeros((w.R, w.T_r, w.H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.zeros((w.R, w.T_r, w.k), dtype=torch.int64, device="cuda")
+    lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E)
+    nt = ep.alloc_notify(w.R, w.E)
+    d = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, 0, 64)
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    with pytest.raises(ep.EPError):
+        ep.ep_layout_notify_dispatch(x, idx, w.E, 0, 1, -1, 64, lay, nt, d, ws)
+
+
+def test_single_call_replays_as_a_cuda_graph():
+    from ep_harness import inputs
+    w = synth.scaled(synth.WORKLOADS["skewed"], T_r=24, H=512, num_worst_tokens=32 * 24)
+    cap = w.cap_rows()
+    x_dev, _, idx_dev, _, _, _ = inputs(w)
+    lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E)
+    nt = ep.alloc_notify(w.R, w.E)
+    d = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, cap)
+    for v in d.values():
+        poison_(v)   # rows no replay fills keep it
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    st = status_word()
+
+    def step():
+        ep.ep_layout_notify_dispatch(x_dev, idx_dev, w.E, w.fp8_mode, 1, w.num_worst_tokens, cap,
+                                     lay, nt, d, ws, st)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    from ep_harness import oracle_normal
+    for seed in (7, 8):
+        _, x_host, _, idx, _, _ = inputs(w, seed=seed)
+        x_dev.copy_(torch.from_numpy(x_host.view(np.int16)).cuda().view(torch.bfloat16))
+        idx_dev.copy_(torch.from_numpy(idx).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert ep.ep_read_status(st) == ep.EP_OK
+        # rows an earlier replay filled may be unused now: compare the valid ones
+        _, _, ref, _ = oracle_normal(x_host, idx, w.E, 1, w.fp8_mode, cap_rows=cap,
+                                     num_worst_tokens=w.num_worst_tokens)
+        assert np.array_equal(np_(d["combine_idx"]), ref["combine_idx"])
+        assert np.array_equal(np_(d["recv_src_idx"]), ref["recv_src_idx"])
+        rows = np.nonzero(ref["recv_src_idx"].reshape(-1) >= 0)[0]
+        got_x = np_(d["recv_x"]).reshape(w.R * cap, -1)
+        assert np.array_equal(got_x[rows], ref["recv_x"].reshape(w.R * cap, -1)[rows])
+        r_idx, row_idx = np.divmod(rows, cap)
+        gs = np_(d["recv_scales"])
+        assert np.array_equal(gs[r_idx, :, row_idx], ref["recv_scales"][r_idx, :, row_idx])
