@@ -550,6 +550,27 @@ def oracle_step(w, x_bits, idx, wts, y_rows, tokens_per_rank: int):
     return w.R * tokens_per_rank
 
 
+class one_core:
+    """Pin this process to one of its allowed CPUs for the oracle's timing
+    (it is single-threaded; the pin makes the core count exact), then
+    restore the previous affinity."""
+
+    def __enter__(self):
+        self.saved = None
+        if hasattr(os, "sched_getaffinity"):
+            try:
+                self.saved = os.sched_getaffinity(0)
+                os.sched_setaffinity(0, {min(self.saved)})
+            except OSError:
+                self.saved = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+        return False
+
+
 def cpu_baseline(w, budget_s: float = 12.0):
     import numpy as np
 
@@ -561,17 +582,18 @@ def cpu_baseline(w, budget_s: float = 12.0):
     sub = synth.scaled(w, T_r=tpr)
     x_bits = synth.activations(sub)
     y_rows = synth.expert_outputs(w.R * tpr * w.k, w.H)
-    done, t0, reps = 0, time.perf_counter(), 0
-    while True:
-        done += oracle_step(w, x_bits, idx, wts, y_rows, tpr)
-        reps += 1
-        if time.perf_counter() - t0 >= budget_s or reps >= 500:
-            break
-    el = time.perf_counter() - t0
+    with one_core():
+        done, t0, reps = 0, time.perf_counter(), 0
+        while True:
+            done += oracle_step(w, x_bits, idx, wts, y_rows, tpr)
+            reps += 1
+            if time.perf_counter() - t0 >= budget_s or reps >= 500:
+                break
+        el = time.perf_counter() - t0
     return {"value": done / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": (f"{reps} x oracle dispatch+combine of the first {tpr} tokens of each of "
                        f"the {w.R} ranks ({w.R * tpr} tokens, 1/{w.T_r // tpr} of the workload), "
-                       f"single-threaded C, {el:.1f} s")}
+                       f"single-threaded C pinned to one core, {el:.1f} s")}
 
 
 # ---------------------------------------------------------------- main
@@ -590,16 +612,18 @@ def run_reference(args, rank, world):
     sub = synth.scaled(w, T_r=tpr)
     x_bits = synth.activations(sub)
     y_rows = synth.expert_outputs(w.R * tpr * w.k, w.H)
-    for _ in range(args.warmup):
-        oracle_step(w, x_bits, idx, wts, y_rows, tpr)
     times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        n = oracle_step(w, x_bits, idx, wts, y_rows, tpr)
-        times.append(time.perf_counter() - t0)
+    with one_core():
+        for _ in range(args.warmup):
+            oracle_step(w, x_bits, idx, wts, y_rows, tpr)
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            n = oracle_step(w, x_bits, idx, wts, y_rows, tpr)
+            times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
     value = n / (ms / 1e3)
-    sample = (f"oracle (single-threaded C) dispatch+combine of the first {tpr} tokens of each "
+    sample = (f"oracle (single-threaded C, pinned to one core) dispatch+combine of the first "
+              f"{tpr} tokens of each "
               f"of the {w.R} ranks per step ({n} tokens)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
