@@ -739,7 +739,8 @@ def run_ours(args, rank, world, local_rank):
         dom = "dispatch"
     kern = {"combine": "k_combine", "dispatch": "k_ll_fused" if runner.ll else "k_scatter"}[dom]
     src = os.path.join(ROOT, "combine_get_dispatch_gb300", "csrc",
-                       "combine.cu" if dom == "combine" else "dispatch.cu")
+                       "combine.cu" if dom == "combine"
+                       else ("ll_fused.cu" if runner.ll else "dispatch.cu"))
     achieved = res[f"{dom}_gbs"]
     roofline = {"bound": "hbm", "kernel": kern, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
