@@ -40,6 +40,27 @@ int grid_cap(int ctas_per_sm) {
   return budget > 0 ? std::min(budget, sms) : sms * ctas_per_sm;
 }
 
+int device_view(void* p, void** dev) {
+  *dev = p;
+  if (p == nullptr) return EP_OK;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_INVALID_ARG;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return EP_OK;
+    case cudaMemoryTypeHost:
+      if (a.devicePointer == nullptr) return EP_ERR_INVALID_ARG;
+      *dev = a.devicePointer;
+      return EP_OK;
+    default:
+      return EP_ERR_INVALID_ARG;
+  }
+}
+
 bool sm_budget_set() { return g_sm_budget.load(std::memory_order_relaxed) > 0; }
 
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }

@@ -177,7 +177,9 @@ extern "C" int ep_combine(const void* y, const float* topk_weights, const int32_
   p.T = (int64_t)R * T_r;
   p.H = H;
   p.k = k;
-  p.out = static_cast<uint8_t*>(out);
+  void* out_dev = nullptr;   // device memory, or pinned host memory written across the link
+  if (ep_host::device_view(out, &out_dev) != EP_OK) return EP_ERR_INVALID_ARG;
+  p.out = static_cast<uint8_t*>(out_dev);
   p.status = status;
   return ep::launch_combine(p, static_cast<cudaStream_t>(stream));
 }
@@ -196,7 +198,9 @@ extern "C" int ep_ll_combine(const void* y, const float* topk_weights, const int
   p.T = (int64_t)R * T_r;
   p.H = H;
   p.k = k;
-  p.out = static_cast<uint8_t*>(out);
+  void* out_dev = nullptr;   // device memory, or pinned host memory written across the link
+  if (ep_host::device_view(out, &out_dev) != EP_OK) return EP_ERR_INVALID_ARG;
+  p.out = static_cast<uint8_t*>(out_dev);
   p.status = status;
   return ep::launch_combine(p, static_cast<cudaStream_t>(stream));
 }
@@ -217,7 +221,9 @@ extern "C" int ep_rank_combine(const void* y, const int32_t* combine_idx, int R,
   p.T = (int64_t)R * T_r;
   p.H = H;
   p.k = k;
-  p.out = static_cast<uint8_t*>(out);
+  void* out_dev = nullptr;   // device memory, or pinned host memory written across the link
+  if (ep_host::device_view(out, &out_dev) != EP_OK) return EP_ERR_INVALID_ARG;
+  p.out = static_cast<uint8_t*>(out_dev);
   p.status = status;
   return ep::launch_combine(p, static_cast<cudaStream_t>(stream));
 }

@@ -289,6 +289,11 @@ int num_sms();   // SMs of the current device
 // while an SM budget is set (ep_set_num_sms), one CTA on each of that many.
 int grid_cap(int ctas_per_sm);
 bool sm_budget_set();
+// The device address of a buffer a kernel may write: device or managed
+// memory as it is, pinned host memory through its mapped device view (the
+// kernel then writes across the host link); EP_ERR_INVALID_ARG for memory
+// the GPU cannot address (pageable host memory), so nothing is launched.
+int device_view(void* p, void** dev);
 void count_launch(int n = 1);
 int check_launch();   // EP_OK or EP_ERR_CUDA after a launch
 // Opt a kernel into `bytes` of dynamic shared memory on the current device

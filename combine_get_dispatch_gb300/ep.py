@@ -135,6 +135,19 @@ def _need(t: torch.Tensor | None, dtype, shape=None, name="tensor", optional=Fal
         raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def _need_out(t: torch.Tensor, dtype, shape, name="out"):
+    """A combine's output: a CUDA tensor, or a pinned host tensor that the
+    kernel writes across the host link."""
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
 def _check(rc: int, where: str):
     if rc != EP_OK:
         raise EPError(rc, where)
@@ -301,7 +314,7 @@ def ep_combine(y, topk_weights, combine_idx, cap_rows, out, status=None, stream=
     _need(y, torch.bfloat16, (R, cap_rows, H), "y")
     _need(topk_weights, torch.float32, (R, T_r, k), "topk_weights")
     _need(combine_idx, torch.int32, (R, T_r, k), "combine_idx")
-    _need(out, torch.bfloat16, (R, T_r, H), "out")
+    _need_out(out, torch.bfloat16, (R, T_r, H))
     _need(status, torch.int32, (1,), "status", optional=True)
     rc = load().ep_combine(_ptr(y), _ptr(topk_weights), _ptr(combine_idx), R, T_r, H, k, cap_rows,
                            _ptr(out), _ptr(status), _stream(stream))
@@ -347,7 +360,7 @@ def ep_ll_combine(y, topk_weights, combine_idx, num_experts, max_tokens_per_rank
     _need(y, torch.bfloat16, (R, E_l, R * max_tokens_per_rank, H), "y")
     _need(topk_weights, torch.float32, (R, T_r, k), "topk_weights")
     _need(combine_idx, torch.int32, (R, T_r, k), "combine_idx")
-    _need(out, torch.bfloat16, (R, T_r, H), "out")
+    _need_out(out, torch.bfloat16, (R, T_r, H))
     _need(status, torch.int32, (1,), "status", optional=True)
     rc = load().ep_ll_combine(_ptr(y), _ptr(topk_weights), _ptr(combine_idx), R, T_r, H, E, k,
                               max_tokens_per_rank, _ptr(out), _ptr(status), _stream(stream))
@@ -392,7 +405,7 @@ def ep_rank_combine(y, combine_idx, cap_rows, out, status=None, stream=None):
     H = out.shape[2]
     _need(y, torch.bfloat16, (R, cap_rows, H), "y")
     _need(combine_idx, torch.int32, (R, T_r, k), "combine_idx")
-    _need(out, torch.bfloat16, (R, T_r, H), "out")
+    _need_out(out, torch.bfloat16, (R, T_r, H))
     _need(status, torch.int32, (1,), "status", optional=True)
     rc = load().ep_rank_combine(_ptr(y), _ptr(combine_idx), R, T_r, H, k, cap_rows, _ptr(out),
                                 _ptr(status), _stream(stream))

@@ -183,6 +183,12 @@ int ep_dispatch(const void* x, const int64_t* topk_idx, const int32_t* slot_rank
                 int32_t* recv_src_idx, int32_t* combine_idx, void* workspace,
                 size_t workspace_bytes, int32_t* status, void* stream);
 
+/* Output of the combines (ep_combine, ep_ll_combine, ep_rank_combine): `out`
+ * is device memory or pinned host memory (cudaHostAlloc, cudaHostRegister):
+ * the kernel then writes the result straight across the host link, with no
+ * separate copy.  Pageable host memory is refused (EP_ERR_INVALID_ARG,
+ * nothing launched).  Every other buffer of every call is device memory. */
+
 /* Normal-mode combine (§1.1, §2.3: dispatch walked backwards):
  *   out[i][t][:] = bf16_rn( fp32 fma chain over j = 0..k-1 of
  *                           topk_weights[i][t][j] * y[combine_idx[i][t][j]][:] )

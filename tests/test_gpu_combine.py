@@ -159,3 +159,37 @@ def test_combine_special_weights_and_masks():
     ep.ep_combine(d["recv_x"], wts_dev, cidx, cap, out, st)
     assert ep.ep_read_status(st) == ep.EP_ERR_INVALID_ARG
     assert np.all(np_(out)[0, 1] == 0)
+
+
+def test_combine_writes_pinned_host_output_directly():
+    """out may be pinned host memory: the combine writes the result across
+    the host link with no copy; bit-identical to a device output.  Pageable
+    host memory is refused before any launch."""
+    import ctypes
+    w = synth.scaled(synth.WORKLOADS["decode"], T_r=32, H=1024)
+    x_dev, _, idx_dev, _, wts_dev, _ = inputs(w)
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, w.fp8_mode)
+    S = w.R * w.max_tokens_per_rank
+    y = _expert_outputs_dev(w.E * S, w.H).view(w.R, w.E_l, S, w.H)
+    out_dev = torch.empty_like(x_dev)
+    out_host = torch.empty(x_dev.shape, dtype=torch.bfloat16).pin_memory()
+    ep.ep_ll_combine(y, wts_dev, d["combine_idx"], w.E, w.max_tokens_per_rank, out_dev)
+    ep.ep_ll_combine(y, wts_dev, d["combine_idx"], w.E, w.max_tokens_per_rank, out_host)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))
+    # rank-level and normal combines take the same path for `out`
+    cap = S
+    yr = y.reshape(w.R, -1, w.H)[:, :cap].contiguous()
+    cidx = torch.where(d["combine_idx"] >= 0, d["combine_idx"] % cap, d["combine_idx"])
+    cidx = cidx.to(torch.int32).contiguous()
+    ep.ep_rank_combine(yr, cidx, cap, out_dev)
+    ep.ep_rank_combine(yr, cidx, cap, out_host)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))
+    pageable = np.empty(out_dev.numel(), np.uint16)
+    L = ep.load()
+    rc = L.ep_ll_combine(ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(wts_dev.data_ptr()),
+                         ctypes.c_void_p(d["combine_idx"].data_ptr()), w.R, w.T_r, w.H, w.E, w.k,
+                         w.max_tokens_per_rank, ctypes.c_void_p(pageable.ctypes.data), None,
+                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == ep.EP_ERR_INVALID_ARG
