@@ -10,12 +10,24 @@
  *   §4.3 EPHandle (psum_num_recv_tokens_per_expert), §4.6 V2 fused notify.
  *
  * Conventions shared by every entry point
- *  - Pointers are DEVICE pointers unless stated otherwise; the caller owns
- *    and allocates every buffer.  No entry point allocates memory.
+ *  - Pointers are DEVICE pointers unless stated otherwise (the combines'
+ *    `out` may be pinned host memory); the caller owns and allocates every
+ *    buffer.  No entry point allocates memory.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every call is stream-ordered and asynchronous, except
- *    ep_notify_dispatch when it is given host counters (it then waits on the
- *    host, bounded by timeout_ms), ep_read_status and ep_host_wait_counters.
+ *    ep_notify_dispatch / ep_layout_notify when given host counters (they
+ *    then wait on the host, bounded by timeout_ms), ep_read_status and
+ *    ep_host_wait_counters.
+ *  - Entry points: layout (ep_get_dispatch_layout, ..._no_alloc), notify
+ *    (ep_notify_dispatch), both in one launch (ep_layout_notify), normal
+ *    dispatch (ep_dispatch; fixed shape with layout + notify in one call:
+ *    ep_layout_notify_dispatch) and combine (ep_combine), low-latency
+ *    dispatch / combine (ep_ll_dispatch, ep_ll_combine, ep_clean_ll_buffer),
+ *    the once-per-rank layout (ep_rank_ids, ep_rank_recv_topk,
+ *    ep_rank_combine), the SM budget (ep_set_num_sms, ep_get_num_sms), the
+ *    kernels' number formats (ep_format_e4m3, ep_format_bf16) and plumbing
+ *    (ep_workspace_size, ep_read_status, ep_host_wait_counters,
+ *    ep_launch_count, ep_error_string).
  *  - Return value: EP_OK, or the first argument / launch error found on the
  *    host (nothing was launched when a validation error is returned).
  *  - `status` (int32 device word, may be NULL): kernels record the first
