@@ -46,8 +46,8 @@ constexpr int kQuantWarps = 12;          // FP8: warps owning (loading, quantisi
                                          // other 4 issue the bulk stores as units are quantised
 constexpr int kFusedMaxPerWarp = 8;      // units per warp
 constexpr int kFusedPiece = 1024;        // channels per unit
-constexpr int kEarlyUnits = 1;           // units per warp loaded with the ids; the rest once
-                                         // the ids have landed
+constexpr int kEarlyUnits = 1;           // units per warp loaded with the ids; the rest right
+                                         // after every thread's id loads are out
 constexpr int kRankWarps = 4;            // the last warps: rank the CTA's own slots (FP8: the
                                          // store warps)
 constexpr int kRankIdsPerLane = 8;
@@ -245,9 +245,9 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
 
   // ---- 0. every id up to the end of the own range goes out first: the CTA
   //      counts the ids before its range itself (their per-expert counts are
-  //      its prefix), so it waits for no other CTA.  Only kEarlyUnits pieces
-  //      per warp follow them now: ~30 MB of reads in flight grid-wide would
-  //      hold the ids back by microseconds.
+  //      its prefix), so it waits for no other CTA.  kEarlyUnits pieces per
+  //      warp follow at once, the rest after the block barrier below, when
+  //      every thread's id loads are out ahead of them.
   constexpr int kScanPairs = kScanIdsPerThread / 2;   // 16-byte id loads per thread per pass
   constexpr int kPassIds = 2 * kThreads * kScanPairs;
   longlong2 vs[kScanPairs];
@@ -282,6 +282,11 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   for (int i = tid; i < (1 + kRankWarps) * p.E; i += kThreads) s_P[i] = 0;   // s_P, s_cnt
   if (tid == 0) s_units_ok = 1;
   __syncthreads();
+  // every thread's id loads are issued now: the rest of the pieces queue
+  // behind them (issued any earlier, a piece could go out ahead of another
+  // thread's ids and hold them back), landing while the ids are counted
+  if (nm > 0 && lane == 0)
+    for (int32_t m = min(nm, kEarlyUnits); m < nm; ++m) load_unit(m);
 
   // ---- 1. per-expert counts of the ids before the own range, and the own ids
   {
@@ -308,8 +313,6 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
     if (bad) set_status(p.status, EP_ERR_INVALID_ARG);
   }
   __syncthreads();
-  if (nm > 0 && lane == 0)   // the ids are in: the rest of the pieces may queue now
-    for (int32_t m = min(nm, kEarlyUnits); m < nm; ++m) load_unit(m);
 
   // ---- 2. the rank warps rank the own slots among themselves (ballots), turn
   //      the per-warp counts into warp starts after the prefix and write the
