@@ -708,6 +708,13 @@ extern "C" int ep_layout_notify_dispatch(
   int rc = ep::check_common(R, T_r, H, E, k, fp8_mode);
   if (rc != EP_OK) return rc;
   if (workspace_bytes < ep_workspace_size(R, T_r, k, E, H)) return EP_ERR_INVALID_ARG;
+  // the dispatch's own argument checks, before anything is launched
+  const bool fp8 = fp8_mode != EP_FP8_NONE;
+  if (cap_rows < 0 || (int64_t)R * cap_rows > INT32_MAX || !recv_src_idx ||
+      (T_r > 0 && (!x || !combine_idx)) || (cap_rows > 0 && !recv_x) ||
+      (fp8 && cap_rows > 0 && !recv_scales) || !ep_host::aligned16(x) ||
+      !ep_host::aligned16(recv_x) || !ep_host::aligned16(workspace))
+    return EP_ERR_INVALID_ARG;
   rc = ep::layout_notify(topk_idx, R, T_r, k, E, expert_alignment, num_worst_tokens,
                          num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank, slot_rank,
                          rank_prefix_matrix, expert_prefix, num_recv_tokens_per_expert, psum,

@@ -241,3 +241,30 @@ def test_single_call_reports_invalid_ids():
     idx_dev[0, 0, 0] = w.E + 5
     lay, nt, d, st, cap = _single_call(w, x_dev, idx_dev, w.fp8_mode, 1)
     assert ep.ep_read_status(st) == ep.EP_ERR_INVALID_ARG
+
+
+def test_single_call_validates_everything_before_launching():
+    """A bad dispatch argument is refused before the layout kernel runs:
+    the layout outputs keep their poison."""
+    w = synth.scaled(synth.WORKLOADS["skewed"], T_r=8, H=512, num_worst_tokens=32 * 8)
+    x = torch.zeros((w.R, w.T_r, w.H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.zeros((w.R, w.T_r, w.k), dtype=torch.int64, device="cuda")
+    lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E)
+    nt = ep.alloc_notify(w.R, w.E)
+    d = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, 16)
+    for v in lay.values():
+        poison_(v)
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    import ctypes
+    L = ep.load()
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    rc = L.ep_layout_notify_dispatch(
+        P(x), P(idx), w.R, w.T_r, w.H, w.E, w.k, w.fp8_mode, 1, w.num_worst_tokens, -1,
+        P(lay["num_tokens_per_rank"]), P(lay["num_tokens_per_expert"]), P(lay["is_token_in_rank"]),
+        P(lay["slot_rank"]), P(nt["rank_prefix_matrix"]), P(nt["expert_prefix"]),
+        P(nt["num_recv_tokens_per_expert"]), P(nt["psum"]), P(d["recv_x"]), P(d["recv_scales"]),
+        P(d["recv_src_idx"]), P(d["combine_idx"]), P(ws), ws.numel(), None,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc == ep.EP_ERR_INVALID_ARG
+    assert np.all(np_(lay["num_tokens_per_rank"]).view(np.uint8) == 0x5A)
