@@ -88,3 +88,43 @@ def test_random_low_latency_shapes(seed):
     ref = _oracle_combine_rows(y.reshape(-1, H), wts, np_(d["combine_idx"]), H)
     assert ref["rc"] == oracle.OK
     assert_bf16_close(np_(out), ref["out"])
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_once_per_rank_shapes(seed):
+    from test_gpu_rank import _compare, _gpu_rank_path
+    rng, R, T_r, H, E, k, fp8 = _shape(200 + seed)
+    idx, wts, x_host = _inputs(rng, R, T_r, H, E, k)
+    g = _gpu_rank_path(to_dev_bf16(x_host), torch.from_numpy(idx).cuda(),
+                       torch.from_numpy(wts).cuda(), E, fp8)
+    if T_r == 0:   # nothing to place: only the status
+        assert ep.ep_read_status(g["status"]) == ep.EP_OK
+        return
+    _compare(x_host, idx, wts, E, fp8, g)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_single_call_fixed_shapes(seed):
+    from ep_harness import poison_, status_word
+    rng, R, T_r, H, E, k, fp8 = _shape(300 + seed)
+    idx, wts, x_host = _inputs(rng, R, T_r, H, E, k)
+    A = int(rng.choice([1, 4, 128]))
+    nwt = R * T_r + int(rng.integers(0, 5))
+    cap = max(1, nwt * min(k, E // R))
+    # the worst case of the fixed shape, plus the alignment padding of every segment
+    cap += (E // R) * (A - 1)
+    idx_dev = torch.from_numpy(idx).cuda()
+    x_dev = to_dev_bf16(x_host)
+    lay = ep.alloc_layout(R, T_r, k, E)
+    nt = ep.alloc_notify(R, E)
+    d = ep.alloc_dispatch(R, T_r, H, k, fp8, cap)
+    for v in list(lay.values()) + list(nt.values()) + list(d.values()):
+        poison_(v)
+    ws = ep.alloc_workspace(R, T_r, k, E, H)
+    st = status_word()
+    ep.ep_layout_notify_dispatch(x_dev, idx_dev, E, fp8, A, nwt, cap, lay, nt, d, ws, st)
+    torch.cuda.synchronize()
+    assert ep.ep_read_status(st) == ep.EP_OK
+    w = synth.Workload("rand", R=R, T_r=T_r, H=H, E=E, k=k, routing="uniform", mode="normal",
+                       fp8_mode=fp8, num_worst_tokens=nwt)
+    _compare_full(w, x_host, idx, d, cap, A)
