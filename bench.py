@@ -217,7 +217,7 @@ class Runner:
             self.nt = ep.alloc_notify(w.R, w.R, device=device)
             self.host_rows = torch.empty(w.R, dtype=torch.int64).pin_memory()
             self._layout_notify()
-            self.cap = int(self.host_rows.max())
+            self.cap = (int(self.host_rows.max()) + 15) // 16 * 16
             self.buf = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, self.cap, device=device)
             self.rtk = torch.empty((w.R, self.cap, w.k), dtype=torch.int64, device=device)
             self.rtw = torch.empty((w.R, self.cap, w.k), dtype=torch.float32, device=device)
@@ -230,9 +230,9 @@ class Runner:
             self.host_rows = torch.empty(w.R, dtype=torch.int64).pin_memory()
             if w.num_worst_tokens >= 0:
                 self.cap = w.cap_rows()
-            else:   # size the receive buffers from one handshake (as the caller would)
-                self._layout_notify()
-                self.cap = int(self.host_rows.max())
+            else:   # size the receive buffers from one handshake (as the caller would),
+                self._layout_notify()   # padded to a multiple of 16 rows
+                self.cap = (int(self.host_rows.max()) + 15) // 16 * 16
             self.buf = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, self.cap, device=device)
             if with_combine:
                 self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(

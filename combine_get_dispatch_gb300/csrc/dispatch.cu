@@ -404,6 +404,59 @@ __device__ __forceinline__ void scale_row_to_columns(const ScaleColParams& p, in
   }
 }
 
+// ue8m0, rows [row0, row0 + 4) of segment seg (row0 % 4 == 0), of which
+// rows row0 + [lo, hi) hold tokens: the four rows' scale bytes of a block
+// are adjacent in its column, so a full quad is one 4-byte store per block
+// (a warp writes 128 consecutive bytes per instruction instead of 32); a
+// partial quad at a segment edge writes its bytes one by one.
+__device__ __forceinline__ void scale_quad_to_columns(const ScaleColParams& p, int64_t seg,
+                                                      int64_t row0, int lo, int hi) {
+  int64_t src[4];
+  bool ok[4];
+  bool full = lo == 0 && hi == 4;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    src[u] = (u >= lo && u < hi) ? __ldg(&p.src_idx[seg * p.seg_rows + row0 + u]) : -1;
+    ok[u] = src[u] >= 0 && src[u] < p.T;
+    full &= ok[u];
+  }
+  const int ngrp = p.row_bytes / 16;
+  for (int g0 = 0; g0 < ngrp; g0 += 2) {
+    uint4 v[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int gg = 0; gg < 2; ++gg)
+        v[u][gg] = (ok[u] && g0 + gg < ngrp)
+                       ? __ldg(reinterpret_cast<const uint4*>(p.scale_rows + src[u] * p.row_bytes) +
+                               g0 + gg)
+                       : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int gg = 0; gg < 2; ++gg) {
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int b = (g0 + gg) * 16 + t;
+        if (b >= p.nb) break;
+        uint32_t c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t w = t < 4 ? v[u][gg].x : t < 8 ? v[u][gg].y : t < 12 ? v[u][gg].z : v[u][gg].w;
+          c[u] = (w >> (8 * (t & 3))) & 0xffu;
+        }
+        const int64_t o = (seg * p.nb + b) * p.seg_rows + row0;
+        uint8_t* out = static_cast<uint8_t*>(p.out);
+        if (full) {
+          *reinterpret_cast<uint32_t*>(out + o) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (ok[u]) out[o + u] = (uint8_t)c[u];
+        }
+      }
+    }
+  }
+}
+
 template <bool kLL, int kEs>
 __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColParams p) {
   if (kLL) {
@@ -411,6 +464,11 @@ __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColPara
     const int64_t n_seg = p.n_rows / p.seg_rows;
     for (int64_t e = blockIdx.x; e < n_seg; e += gridDim.x) {   // one expert per CTA pass
       const int64_t lim = min((int64_t)max(__ldg(&p.recv_count[e]), 0), p.seg_rows);
+      if (kEs == 1 && p.quad) {
+        for (int64_t q = threadIdx.x; q * 4 < lim; q += kScaleColThreads)
+          scale_quad_to_columns(p, e, q * 4, 0, (int)min((int64_t)4, lim - q * 4));
+        continue;
+      }
       for (int64_t row = threadIdx.x; row < lim; row += kScaleColThreads) {
         const int64_t f = e * p.seg_rows + row;
         const int64_t src = __ldg(&p.src_idx[f]);
@@ -422,7 +480,9 @@ __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColPara
   if (p.tables_after_wait) pdl_wait();
   __shared__ int32_t s_base[kMaxE + 1];   // exclusive prefix of the valid rows per segment
   __shared__ int32_t s_start[kMaxE];      // first row of every segment in its rank
+  __shared__ int32_t s_valid[kMaxE];      // quad mode: valid rows of every segment
   __shared__ int32_t s_warp[kScaleColThreads / kWarp];
+  const bool quad = kEs == 1 && p.quad;   // s_base then counts 4-row quads
   constexpr int kPer = (kMaxE + kScaleColThreads - 1) / kScaleColThreads;
   const int tid = threadIdx.x;
   int32_t cnt[kPer];
@@ -437,6 +497,11 @@ __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColPara
       const int64_t room = max((int64_t)0, p.seg_rows - start);
       cnt[u] = (int32_t)min((int64_t)max(__ldg(&p.expert_total[e]), 0), room);
       s_start[e] = (int32_t)min(start, p.seg_rows);
+      if (quad) {
+        s_valid[e] = cnt[u];
+        const int64_t a = s_start[e];
+        cnt[u] = cnt[u] > 0 ? (int32_t)(((a + cnt[u] + 3) >> 2) - (a >> 2)) : 0;
+      }
     }
     sum += cnt[u];
   }
@@ -475,6 +540,13 @@ __global__ void __launch_bounds__(kScaleColThreads) k_scale_columns(ScaleColPara
       else hi = mid;
     }
     const int r = lo / p.E_l;
+    if (quad) {   // quad f - s_base[lo] of the segment's quads
+      const int64_t a = s_start[lo];
+      const int64_t row0 = ((a >> 2) + (f - s_base[lo])) * 4;
+      const int64_t b = a + s_valid[lo];
+      scale_quad_to_columns(p, r, row0, (int)(max(a, row0) - row0), (int)(min(b, row0 + 4) - row0));
+      continue;
+    }
     const int64_t row = (int64_t)s_start[lo] + (f - s_base[lo]);
     const int64_t src = __ldg(&p.src_idx[(int64_t)r * p.seg_rows + row]);
     if (src >= 0 && src < p.T) scale_row_to_columns<kEs>(p, r, row, src);
@@ -681,6 +753,8 @@ static int dispatch_normal(const void* x, const int64_t* topk_idx, const int32_t
   sp.E = E;
   sp.E_l = E / R;
   sp.out = recv_scales;
+  sp.quad = fp8_mode == EP_FP8_E4M3_UE8M0 && cap_rows % 4 == 0 &&
+            (reinterpret_cast<uintptr_t>(recv_scales) & 3) == 0;
   sp.tables_after_wait = pdl;
   return ep::launch_scale_columns(sp, false, fp8_mode, s);
 }

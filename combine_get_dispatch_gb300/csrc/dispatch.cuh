@@ -104,6 +104,8 @@ struct ScaleColParams {
   const int64_t* psum;         // normal mode: [R][E_l + 1] segment starts
   const int32_t* expert_total; // normal mode: [E] rows of every expert (unaligned)
   int E, E_l;
+  bool quad;                   // ue8m0 with seg_rows % 4 == 0 and out 4-byte aligned: a
+                               // thread writes 4 consecutive rows (one word per block)
   bool tables_after_wait;      // normal mode: the segment tables may still be in the making
                                // when this kernel starts (the scatter itself was a dependent
                                // launch of layout + notify): read them after the wait

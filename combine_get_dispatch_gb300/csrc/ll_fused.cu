@@ -676,5 +676,7 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
   sp.src_idx = packed_recv_src_info;
   sp.recv_count = recv_count;
   sp.out = packed_recv_scales;
+  sp.quad = fp8_mode == EP_FP8_E4M3_UE8M0 && seg_rows % 4 == 0 &&
+            (reinterpret_cast<uintptr_t>(packed_recv_scales) & 3) == 0;
   return ep::launch_scale_columns(sp, true, fp8_mode, s);
 }
