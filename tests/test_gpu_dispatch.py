@@ -234,18 +234,20 @@ def test_handle_reuse_across_dispatches(fp8_mode):
         _compare_full(w, x_host, idx, d, cap, 1)
 
 
-@pytest.mark.parametrize("pad,A", [(16, 1), (16, 4), (2, 1), (0, 128)])
-def test_ue8m0_scale_columns_quad_and_byte_paths(pad, A):
-    """The ue8m0 column pass writes 4 rows per thread (one word per block)
-    when cap_rows is a multiple of 4, byte by byte otherwise; segment edges
-    inside a quad take the byte path.  Both must give the oracle's scales."""
-    w = synth.scaled(synth.WORKLOADS["large"], T_r=90, fp8_mode=2)
+@pytest.mark.parametrize("fp8_mode", [1, 2])
+@pytest.mark.parametrize("pad,A", [(16, 1), (16, 4), (2, 1), (1, 1), (0, 128)])
+def test_scale_columns_quad_and_single_row_paths(pad, A, fp8_mode):
+    """With ue8m0 scales the column pass writes 4 rows per thread (one 4-byte
+    store per block) when cap_rows is a multiple of 4, row by row otherwise;
+    segment edges inside a quad store byte by byte.  fp32 scales always go
+    row by row.  Every path must give the oracle's scales."""
+    w = synth.scaled(synth.WORKLOADS["large"], T_r=90, fp8_mode=fp8_mode)
     x_dev, x_host, idx_dev, idx, _, _ = inputs(w, seed=3)
     lay = gpu_layout(idx_dev, w.E)
     nt = gpu_notify(lay, w.E, A, -1)
-    _, _, _, cap = oracle_normal(x_host, idx, w.E, A, 2)
+    _, _, _, cap = oracle_normal(x_host, idx, w.E, A, fp8_mode)
     cap = (cap + 15) // 16 * 16 + pad if pad == 16 else cap + pad
-    d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, 2, cap)
+    d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, fp8_mode, cap)
     torch.cuda.synchronize()
     assert ep.ep_read_status(d["status"]) == ep.EP_OK
     _compare_full(w, x_host, idx, d, cap, A)
