@@ -558,8 +558,8 @@ static int launch_scale_columns_t(const ScaleColParams& p, cudaStream_t stream) 
   dim3 grid;
   if (kLL) {
     grid = dim3((unsigned)std::min<int64_t>(p.n_rows / p.seg_rows, ep_host::grid_cap(8)));
-  } else {   // the valid rows are known only on the device: at most T * k
-    const int64_t want = (p.T * 16 + kScaleColThreads - 1) / kScaleColThreads;
+  } else {   // the valid rows are known only on the device: bounded by max_items
+    const int64_t want = (p.max_items + kScaleColThreads - 1) / kScaleColThreads;
     grid = dim3((unsigned)std::max<int64_t>(
         1, std::min<int64_t>(want, (int64_t)ep_host::grid_cap(8))));
   }
@@ -756,6 +756,9 @@ static int dispatch_normal(const void* x, const int64_t* topk_idx, const int32_t
   sp.quad = fp8_mode == EP_FP8_E4M3_UE8M0 && cap_rows % 4 == 0 &&
             (reinterpret_cast<uintptr_t>(recv_scales) & 3) == 0;
   sp.tables_after_wait = pdl;
+  // at most T * k valid rows; a segment's quads cover its rows plus at most
+  // one partial quad at each end
+  sp.max_items = sp.quad ? (p.T * k + 3) / 4 + 2 * (int64_t)E : p.T * k;
   return ep::launch_scale_columns(sp, false, fp8_mode, s);
 }
 

@@ -98,6 +98,8 @@ struct ScaleColParams {
   int64_t T;
   int64_t seg_rows;
   int64_t n_rows;              // rows of the receive buffer (segments * seg_rows)
+  int64_t max_items;           // normal mode: bound on the flat loop's items (valid rows,
+                               // or 4-row quads), which sizes the grid
   const int32_t* src_idx;      // token of every receive row, -1 = none (normal mode)
   const int32_t* recv_count;   // low-latency mode: rows per expert segment (src_idx
                                // is only defined below it)
