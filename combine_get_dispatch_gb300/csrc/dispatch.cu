@@ -711,6 +711,8 @@ static int dispatch_normal(const void* x, const int64_t* topk_idx, const int32_t
     return EP_ERR_INVALID_ARG;
   if (!ep_host::aligned16(x) || !ep_host::aligned16(recv_x) || !ep_host::aligned16(workspace))
     return EP_ERR_INVALID_ARG;
+  if (fp8_mode == EP_FP8_E4M3_F32_SCALE && reinterpret_cast<uintptr_t>(recv_scales) % 4 != 0)
+    return EP_ERR_INVALID_ARG;   // fp32 scales are stored as 4-byte words
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ep::ScatterParams p{};
   p.x = static_cast<const uint8_t*>(x);

@@ -592,6 +592,8 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
   if (!ep_host::aligned16(x) || !ep_host::aligned16(packed_recv_x) ||
       !ep_host::aligned16(workspace))
     return EP_ERR_INVALID_ARG;
+  if (fp8_mode == EP_FP8_E4M3_F32_SCALE && reinterpret_cast<uintptr_t>(packed_recv_scales) % 4 != 0)
+    return EP_ERR_INVALID_ARG;   // fp32 scales are stored as 4-byte words
   if (workspace_bytes < ep_workspace_size(R, T_r, k, E, H)) return EP_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int es = fp8_mode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;

@@ -180,7 +180,8 @@ int ep_layout_notify_dispatch(const void* x, const int64_t* topk_idx, int R, int
  * into rank r's row psum[r][l] + expert_prefix[i][e] + slot_rank[i][t][j].
  *   x            [R, T_r, H] bf16
  *   recv_x       [R, cap_rows, H] bf16 (fp8_mode 0) or E4M3 bytes
- *   recv_scales  [R, H/128, cap_rows] fp32 (mode 1) / uint8 (mode 2); NULL in mode 0
+ *   recv_scales  [R, H/128, cap_rows] fp32 (mode 1, 4-byte aligned) / uint8 (mode 2);
+ *                NULL in mode 0
  *   recv_src_idx [R, cap_rows] int32: i*T_r + t for every filled row, -1 on
  *                alignment padding and past the last row
  *   combine_idx  [R, T_r, k] int32: r*cap_rows + row, -1 for an unused slot
@@ -217,7 +218,8 @@ int ep_combine(const void* y, const float* topk_weights, const int32_t* combine_
  * e = r*E_l + l owns rows [0, recv_count[r][l]) of packed_recv_x[r][l],
  * ordered by (source rank, token, slot); T_r <= max_tokens_per_rank.
  *   packed_recv_x        [R, E_l, R*max_tokens_per_rank, H] bf16 or E4M3
- *   packed_recv_scales   [R, E_l, H/128, R*max_tokens_per_rank] fp32 / uint8
+ *   packed_recv_scales   [R, E_l, H/128, R*max_tokens_per_rank] fp32 (4-byte
+ *                        aligned) / uint8
  *   packed_recv_src_info [R, E_l, R*max_tokens_per_rank] int32: i*T_r + t
  *   layout_range         [R, E_l, R] int64: (offset << 32) | count of source
  *                        rank i's rows inside the segment

@@ -251,3 +251,36 @@ def test_scale_columns_quad_and_single_row_paths(pad, A, fp8_mode):
     torch.cuda.synchronize()
     assert ep.ep_read_status(d["status"]) == ep.EP_OK
     _compare_full(w, x_host, idx, d, cap, A)
+
+
+def test_fp32_scale_buffer_must_be_word_aligned():
+    """fp32 scales are stored as 4-byte words: both dispatches refuse a
+    scale buffer that is not 4-byte aligned before launching anything."""
+    import ctypes
+    w = synth.scaled(synth.WORKLOADS["tiny"], fp8_mode=1)
+    x_dev, _, idx_dev, _, _, _ = inputs(w, seed=5)
+    lay = gpu_layout(idx_dev, w.E)
+    nt = gpu_notify(lay, w.E, 1, -1)
+    R, T_r, H = x_dev.shape
+    k = idx_dev.shape[2]
+    cap = 64
+    out = ep.alloc_dispatch(R, T_r, H, k, 1, cap)
+    ws = ep.alloc_workspace(R, T_r, k, w.E, H)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    P = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + off)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    L = ep.load()
+    rc = L.ep_dispatch(P(x_dev), P(idx_dev), P(lay["slot_rank"]), P(nt["expert_prefix"]),
+                       P(nt["psum"]), R, T_r, H, w.E, k, 1, cap, P(out["recv_x"]),
+                       P(out["recv_scales"], 2), P(out["recv_src_idx"]), P(out["combine_idx"]),
+                       P(ws), ws.numel(), P(status), stream)
+    assert rc == ep.EP_ERR_INVALID_ARG
+    ll = ep.alloc_ll(R, T_r, H, w.E, k, w.max_tokens_per_rank, 1)
+    rc = L.ep_ll_dispatch(P(x_dev), P(idx_dev), R, T_r, H, w.E, k, w.max_tokens_per_rank, 1,
+                          P(ll["packed_recv_x"]), P(ll["packed_recv_scales"], 2),
+                          P(ll["packed_recv_src_info"]), P(ll["layout_range"]),
+                          P(ll["recv_count"]), P(ll["combine_idx"]), P(ws), ws.numel(),
+                          P(status), stream)
+    assert rc == ep.EP_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert int(status.item()) == ep.EP_OK
