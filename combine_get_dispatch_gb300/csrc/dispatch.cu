@@ -792,7 +792,8 @@ extern "C" int ep_layout_notify_dispatch(
   if (cap_rows < 0 || (int64_t)R * cap_rows > INT32_MAX || !recv_src_idx ||
       (T_r > 0 && (!x || !combine_idx)) || (cap_rows > 0 && !recv_x) ||
       (fp8 && cap_rows > 0 && !recv_scales) || !ep_host::aligned16(x) ||
-      !ep_host::aligned16(recv_x) || !ep_host::aligned16(workspace))
+      !ep_host::aligned16(recv_x) || !ep_host::aligned16(workspace) ||
+      (fp8_mode == EP_FP8_E4M3_F32_SCALE && reinterpret_cast<uintptr_t>(recv_scales) % 4 != 0))
     return EP_ERR_INVALID_ARG;
   rc = ep::layout_notify(topk_idx, R, T_r, k, E, expert_alignment, num_worst_tokens,
                          num_tokens_per_rank, num_tokens_per_expert, is_token_in_rank, slot_rank,

@@ -243,9 +243,11 @@ def test_single_call_reports_invalid_ids():
     assert ep.ep_read_status(st) == ep.EP_ERR_INVALID_ARG
 
 
-def test_single_call_validates_everything_before_launching():
-    """A bad dispatch argument is refused before the layout kernel runs:
-    the layout outputs keep their poison."""
+@pytest.mark.parametrize("bad", ["cap_rows", "scale_alignment"])
+def test_single_call_validates_everything_before_launching(bad):
+    """A bad dispatch argument (a negative capacity; fp32 scales not 4-byte
+    aligned) is refused before the layout kernel runs: the layout outputs
+    keep their poison."""
     w = synth.scaled(synth.WORKLOADS["skewed"], T_r=8, H=512, num_worst_tokens=32 * 8)
     x = torch.zeros((w.R, w.T_r, w.H), dtype=torch.bfloat16, device="cuda")
     idx = torch.zeros((w.R, w.T_r, w.k), dtype=torch.int64, device="cuda")
@@ -257,12 +259,15 @@ def test_single_call_validates_everything_before_launching():
     ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
     import ctypes
     L = ep.load()
-    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    P = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + off) if t is not None else None
+    cap = -1 if bad == "cap_rows" else 16
+    off = 2 if bad == "scale_alignment" else 0
+    assert w.fp8_mode == 1   # fp32 scales
     rc = L.ep_layout_notify_dispatch(
-        P(x), P(idx), w.R, w.T_r, w.H, w.E, w.k, w.fp8_mode, 1, w.num_worst_tokens, -1,
+        P(x), P(idx), w.R, w.T_r, w.H, w.E, w.k, w.fp8_mode, 1, w.num_worst_tokens, cap,
         P(lay["num_tokens_per_rank"]), P(lay["num_tokens_per_expert"]), P(lay["is_token_in_rank"]),
         P(lay["slot_rank"]), P(nt["rank_prefix_matrix"]), P(nt["expert_prefix"]),
-        P(nt["num_recv_tokens_per_expert"]), P(nt["psum"]), P(d["recv_x"]), P(d["recv_scales"]),
+        P(nt["num_recv_tokens_per_expert"]), P(nt["psum"]), P(d["recv_x"]), P(d["recv_scales"], off),
         P(d["recv_src_idx"]), P(d["combine_idx"]), P(ws), ws.numel(), None,
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
