@@ -49,9 +49,11 @@ _lib = None
 
 
 def lib() -> ctypes.CDLL:
+    """The oracle library; EP_ORACLE_LIB names another build of it (the
+    mutation tests load copies with a planted mistake this way)."""
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
+        _lib = ctypes.CDLL(os.environ.get("EP_ORACLE_LIB") or build())
         _declare(_lib)
     return _lib
 
