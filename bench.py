@@ -817,6 +817,17 @@ def run_ours(args, rank, world, local_rank):
             del runner
             torch.cuda.empty_cache()
 
+    line = assemble_line(args, world, head, results, clocks, peak, peak_kind)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(results[head][0])
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def assemble_line(args, world, head, results, clocks, peak, peak_kind):
+    """The contract's JSON line from the per-workload measurements (results:
+    name -> (workload, runner, measured dict); the headline first)."""
     w, runner, res = results[head]
     ms = res["step_ms_max"]
     value = world * w.T / (ms * 1e-3)
@@ -889,11 +900,7 @@ def run_ours(args, rank, world, local_rank):
         line["single_call"] = res["single_call"]
     for key in ("step_us_stats", "dispatch_us_stats", "combine_us_stats"):
         line[key] = res[key]
-    if rank == 0:
-        if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(w)
-        print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 def main(argv=None):
