@@ -60,18 +60,26 @@ MUTANTS = {
     "psum_wrong_rank": ("s += num_recv_tokens_per_expert[(int64_t)r * E_l + l];",
                         "s += num_recv_tokens_per_expert[(int64_t)l];", 0),
     "worst_tokens_off_by_one": ("run > num_worst_tokens", "run >= num_worst_tokens", 0),
+    "worst_tokens_check_dropped": (
+        "if (num_worst_tokens >= 0 && run > num_worst_tokens) rc = ORACLE_ERR_CAPACITY;",
+        "if (num_worst_tokens >= 0 && run > num_worst_tokens) rc = ORACLE_OK;", 0),
     # normal dispatch
     "dispatch_drops_source_offset": (
         "psum[(int64_t)r * (E_l + 1) + l] + expert_prefix[(int64_t)i * E + e] + slot_rank[p];",
         "psum[(int64_t)r * (E_l + 1) + l] + slot_rank[p];", 0),
     "dispatch_local_index_transposed": ("int l = (int)(e % E_l);", "int l = (int)(e / R);", 0),
     "dispatch_src_idx_local": ("recv_src_idx[flat] = i * T_r + t;", "recv_src_idx[flat] = t;", 0),
+    "dispatch_capacity_not_reported": (
+        "          combine_idx[p] = -1;\n          rc = ORACLE_ERR_CAPACITY;\n          continue;",
+        "          combine_idx[p] = -1;\n          continue;", 0),
     # low-latency dispatch
     "ll_recv_count_exclusive": ("recv_count[e] = eprefix[(int64_t)R * E + e];",
                                 "recv_count[e] = eprefix[(int64_t)(R - 1) * E + e];", 0),
     "ll_range_fields_swapped": (
         "((int64_t)eprefix[(int64_t)i * E + e] << 32) | (int64_t)ntpe[(int64_t)i * E + e];",
         "((int64_t)ntpe[(int64_t)i * E + e] << 32) | (int64_t)eprefix[(int64_t)i * E + e];", 0),
+    "ll_max_tokens_check_dropped": ("if (R <= 0 || E % R != 0 || T_r > max_tokens_per_rank ||",
+                                    "if (R <= 0 || E % R != 0 ||", 0),
     "ll_row_drops_source_offset": ("int64_t row = (int64_t)eprefix[(int64_t)i * E + e] + slot_rank[p];",
                                    "int64_t row = (int64_t)slot_rank[p];", 0),
     # combine
@@ -80,6 +88,9 @@ MUTANTS = {
                                "acc = acc + ep_oracle_bf16_to_f32(y[(int64_t)f * H + h]);", 0),
     # once-per-rank layout and combine
     "rank_prefix_transposed": ("before += cnt[(int64_t)i * R + r];", "before += cnt[(int64_t)r * R + i];", 0),
+    "rank_capacity_not_reported": (
+        "          combine_idx[base + first] = -1;\n          rc = ORACLE_ERR_CAPACITY;",
+        "          combine_idx[base + first] = -1;", 0),
     "rank_topk_global_index": ("recv_topk_idx[flat * k + j] = on_r ? e - (int64_t)r * E_l : -1;",
                                "recv_topk_idx[flat * k + j] = on_r ? e : -1;", 0),
     "rank_combine_keeps_last": ("acc = acc + ep_oracle_bf16_to_f32(y[(int64_t)f * H + h]);",
