@@ -8,11 +8,13 @@ One step = one pass of the hot path over one batch:
       ep_dispatch + ep_combine.
 Inputs are resident in HBM before the timed region; L2 is flushed (512 MiB
 write) before every step, outside the per-step CUDA events.  The JSON line
-reports the decode workload; the other workloads are measured in the same
-run under "workloads".
+reports the large throughput workload (R=8 x 16384 tokens, H=7168, FP8 ue8m0
+dispatch, bf16 combine: the largest configuration on one GPU); the other
+workloads are measured in the same run under "workloads", each with its own
+roofline object.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workloads decode,prefill,skewed,large]
+                  [--workloads large,decode,prefill,skewed,prefill_v1]
   python bench.py --sm-sweep 8,16,32,64,152 [--workloads ...]   (GB/s per SM
                   under an SM budget; one line per workload and budget)
 
@@ -36,7 +38,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
-HEADLINE = "decode"
+HEADLINE = "large"
 # bench-only workloads: a base workload run through another layout
 # ("rank": the once-per-rank receive layout of V1's normal mode)
 DERIVED = {"prefill_v1": ("prefill", {"mode": "rank"})}
@@ -57,7 +59,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workloads", default="decode,prefill,skewed,large,prefill_v1")
+    ap.add_argument("--workloads", default="large,decode,prefill,skewed,prefill_v1")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     # profiling aids (change the workload; never used for a reported number)
@@ -581,8 +583,12 @@ def measure_e2e(runner, steps, world, flush):
             raise RuntimeError("pipelined end-to-end step: host output differs from the device step")
     h2d = hx.numel() * hx.element_size() + hi.numel() * 8 + hw.numel() * 4
     d2h = ho.numel() * ho.element_size()
+    how = ("the K steps replayed as one CUDA graph" if runner.capturable else
+           "issued eagerly: the step waits on the host for its receive counts")
     return {"ms": pipe_ms, "serial_ms": serial_ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "mode": ("pipelined: next upload and previous download overlap the kernels "
+                     f"(copy streams, double-buffered host I/O, {how}, no L2 flush)")}
 
 
 def kernel_hash(path: str) -> str:
@@ -664,6 +670,13 @@ class one_core:
         return False
 
 
+def oracle_sample_tokens(w) -> int:
+    """Tokens per rank in one oracle sample step: about 512 tokens in all
+    (half a second of the single-threaded oracle at H = 7168), at least one
+    per rank, never more than the workload has."""
+    return max(1, min(w.T_r, 512 // w.R))
+
+
 def cpu_baseline(w, budget_s: float = 12.0):
     import numpy as np
 
@@ -671,7 +684,7 @@ def cpu_baseline(w, budget_s: float = 12.0):
     from combine_get_dispatch_gb300 import synth
     oracle.build()
     idx, wts = synth.routing(w)
-    tpr = max(1, w.T_r // 8) if w.T_r >= 8 else w.T_r
+    tpr = oracle_sample_tokens(w)
     sub = synth.scaled(w, T_r=tpr)
     x_bits = synth.activations(sub)
     y_rows = synth.expert_outputs(w.R * tpr * w.k, w.H)
@@ -701,7 +714,7 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     idx, wts = synth.routing(w)
-    tpr = max(1, w.T_r // 8)
+    tpr = oracle_sample_tokens(w)
     sub = synth.scaled(w, T_r=tpr)
     x_bits = synth.activations(sub)
     y_rows = synth.expert_outputs(w.R * tpr * w.k, w.H)
@@ -721,7 +734,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": workload_desc(w)},
+            "data": "synthetic", "config": config_of(w, args.gpus),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -825,6 +838,37 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+def config_of(w, world: int) -> dict:
+    """The workload's config object (shared by both arms' lines)."""
+    return {"workload": workload_desc(w), "l2": "flushed before every step (512 MiB write)",
+            "parallelism": f"{world} replica(s), {w.R} ranks emulated per GPU",
+            "data_types": ("x bf16 -> " + {0: "bf16", 1: "E4M3 + fp32 scales",
+                                              2: "E4M3 + ue8m0 scales"}[w.fp8_mode]
+                           + " dispatch; y bf16 -> bf16 combine, fp32 accumulate")}
+
+
+def roofline_of(name, w, runner, res, peak, peak_kind, dispatch_only=False):
+    """Roofline object of a workload's dominant kernel (the longer of its
+    dispatch and combine): algorithmic bytes per launch over the CUDA-event
+    time of the launch, against the HBM copy peak; traffic = DRAM bytes per
+    launch from the committed ncu summary while the kernel source is
+    unchanged since it was taken, else null."""
+    dom = "combine" if res["combine_ms"] >= res["dispatch_ms"] else "dispatch"
+    if dispatch_only:
+        dom = "dispatch"
+    kern = {"combine": "k_combine", "dispatch": "k_ll_fused" if runner.ll else "k_scatter"}[dom]
+    src = os.path.join(ROOT, "combine_get_dispatch_gb300", "csrc",
+                       "combine.cu" if dom == "combine"
+                       else ("ll_fused.cu" if runner.ll else "dispatch.cu"))
+    achieved = res[f"{dom}_gbs"]
+    return {"bound": "hbm", "kernel": kern, "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "alg_bytes_per_launch": res[f"{dom}_alg_bytes"],
+            "launch_us": round(res[f"{dom}_ms"] * 1e3, 2),
+            "traffic": load_traffic(kern, name, src)}
+
+
 def assemble_line(args, world, head, results, clocks, peak, peak_kind):
     """The contract's JSON line from the per-workload measurements (results:
     name -> (workload, runner, measured dict); the headline first)."""
@@ -838,42 +882,23 @@ def assemble_line(args, world, head, results, clocks, peak, peak_kind):
         e2e = {"value": world * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": res["e2e"]["h2d_bytes_per_step"],
                "d2h_bytes_per_step": res["e2e"]["d2h_bytes_per_step"], "ms_per_step": e2e_ms,
-               "mode": "pipelined: next upload and previous download overlap the kernels "
-                       "(copy streams, double-buffered host I/O, the K steps replayed as one "
-                       "CUDA graph where the step can be captured, no L2 flush)",
+               "mode": res["e2e"].get("mode", "pipelined"),
                "serial_ms_per_step": serial_ms,
                "serial_value": world * w.T / (serial_ms * 1e-3)}
-    # dominant kernel of the headline step: the one with the larger time
-    dom = "combine" if res["combine_ms"] >= res["dispatch_ms"] else "dispatch"
-    if args.no_combine:
-        dom = "dispatch"
-    kern = {"combine": "k_combine", "dispatch": "k_ll_fused" if runner.ll else "k_scatter"}[dom]
-    src = os.path.join(ROOT, "combine_get_dispatch_gb300", "csrc",
-                       "combine.cu" if dom == "combine"
-                       else ("ll_fused.cu" if runner.ll else "dispatch.cu"))
-    achieved = res[f"{dom}_gbs"]
-    roofline = {"bound": "hbm", "kernel": kern, "achieved": round(achieved, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"{peak_kind} hbm_gbs",
-                "alg_bytes_per_launch": res[f"{dom}_alg_bytes"],
-                "traffic": load_traffic(kern, head, src)}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": workload_desc(w), "l2": "flushed before every step (512 MiB write)",
-                       "parallelism": f"{world} replica(s), {w.R} ranks emulated per GPU",
-                       "data_types": ("x bf16 -> " + {0: "bf16", 1: "E4M3 + fp32 scales",
-                                                         2: "E4M3 + ue8m0 scales"}[w.fp8_mode]
-                                      + " dispatch; y bf16 -> bf16 combine, fp32 accumulate")},
+            "data": "synthetic", "config": config_of(w, world),
             "hbm_gbs": {"dispatch": round(res["dispatch_gbs"], 1),
                         "combine": round(res["combine_gbs"], 1),
                         "dispatch_frac": round(res["dispatch_gbs"] / peak, 4),
                         "combine_frac": round(res["combine_gbs"] / peak, 4)},
             "clocks": clocks, "e2e": e2e, "gpu_launches": res["launches"],
-            "roofline": roofline}
+            "roofline": roofline_of(head, w, runner, res, peak, peak_kind, args.no_combine)}
+    if "wall_s" in res:
+        line["timed_region_s"] = round(res["wall_s"], 4)
     others = {}
-    for name, (wo, _, r) in results.items():
+    for name, (wo, ro, r) in results.items():
         if name == head:
             continue
         others[name] = {
@@ -884,7 +909,8 @@ def assemble_line(args, world, head, results, clocks, peak, peak_kind):
             "dispatch_frac": round(r["dispatch_gbs"] / peak, 4),
             "combine_frac": round(r["combine_gbs"] / peak, 4),
             "layout_notify_ms": round(r["step_ms"] - r["dispatch_ms"] - r["combine_ms"], 4),
-            "gpu_launches": r["launches"]}
+            "gpu_launches": r["launches"],
+            "roofline": roofline_of(name, wo, ro, r, peak, peak_kind, args.no_combine)}
         if r.get("launch_latency_us"):
             others[name]["launch_latency_us"] = r["launch_latency_us"]
         if r.get("single_call"):
@@ -893,7 +919,9 @@ def assemble_line(args, world, head, results, clocks, peak, peak_kind):
             others[name][key] = r[key]
     line["workloads"] = others
     line["kernels_ms"] = {"dispatch": round(res["dispatch_ms"], 5),
-                          "combine": round(res["combine_ms"], 5)}
+                          "combine": round(res["combine_ms"], 5),
+                          "layout_notify": round(res["step_ms"] - res["dispatch_ms"]
+                                                 - res["combine_ms"], 5)}
     if res.get("launch_latency_us"):
         line["launch_latency_us"] = res["launch_latency_us"]
     if res.get("single_call"):

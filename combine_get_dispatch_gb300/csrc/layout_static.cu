@@ -19,7 +19,12 @@
 //    part it uses (a stream-ordered memset, no allocation);
 //  - the first call on a device looks the array's device address up with
 //    cudaGetSymbolAddress (with that device current); make that first call
-//    before any stream capture begins.
+//    before any stream capture begins.  The address is kept for the life of
+//    the process, so the library must not be used on a device after
+//    cudaDeviceReset on it;
+//  - the stream must belong to the current device (the array looked up is
+//    the current device's); a stream of another device is refused with
+//    EP_ERR_INVALID_ARG before anything is launched.
 
 #include <mutex>
 
@@ -75,10 +80,18 @@ extern "C" int ep_get_dispatch_layout_no_alloc(const int64_t* topk_idx, int R, i
   if (!num_tokens_per_rank || !num_tokens_per_expert ||
       (T_r > 0 && (!topk_idx || !is_token_in_rank || !slot_rank)))
     return EP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread) {
+    int cur = -1, sdev = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess) {
+      cudaGetLastError();
+      return EP_ERR_INVALID_ARG;
+    }
+    if (sdev != cur) return EP_ERR_INVALID_ARG;   // scratch of one device, work on another
+  }
   void* scratch = nullptr;
   int rc = scratch_address(&scratch);
   if (rc != EP_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   // start from a clean scratch: ticket / epoch words and look-back words
   if (cudaMemsetAsync(scratch, 0, bytes, s) != cudaSuccess) {
     cudaGetLastError();

@@ -3,6 +3,8 @@
 // the layout + scatter + scale-column kernels of dispatch.cu otherwise
 // (llm-infra-atlas DeepEP article §1.2, §3.2, §4.6).
 
+#include <mutex>
+
 #include "dispatch.cuh"
 
 namespace ep {
@@ -37,9 +39,10 @@ namespace ep {
 // L2 after the first touch) but takes no round trip through another CTA: an
 // exchange of per-chunk counts, read while the x pieces are queued, made
 // every CTA wait for the slowest and for the x queue.
-// All CTAs are resident at once (one per SM, grid = SM count), so the wait
-// at the grid barrier ends; every wait is bounded anyway and gives up with
-// EP_ERR_TIMEOUT.
+// All CTAs are resident at once (one per SM, grid at most the SM count,
+// launched cooperatively, so the runtime starts the grid only when every
+// CTA has an SM), so the wait at the grid barrier ends; every wait is
+// bounded anyway and gives up with EP_ERR_TIMEOUT.
 
 constexpr int kFusedWarps = 16;
 constexpr int kQuantWarps = 12;          // FP8: warps owning (loading, quantising) units; the
@@ -552,15 +555,68 @@ static bool plan_fused(FusedParams& p, int grid) {
   return fused_smem(p) <= kFusedSmemCap;
 }
 
+// Returned by launch_fused when the grid cannot be co-resident (the caller
+// then takes the multi-kernel path); never returned to a user.
+constexpr int kFusedNotLaunched = -1;
+
+// Whether one CTA of k_ll_fused<kMode> with the largest shared-memory size
+// it is planned for fits on an SM of the current device (then any grid of at
+// most one CTA per SM can be co-resident).  Cached per device.
+template <int kMode>
+static bool fused_fits_one_per_sm() {
+  static std::mutex mu;
+  static signed char cached[64] = {0};   // 0 unknown, 1 fits, -1 does not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ll_fused<kMode>, kFusedWarps * kWarp,
+                                                      kFusedSmemCap) != cudaSuccess) {
+      cudaGetLastError();
+      per_sm = 0;
+    }
+    cached[dev] = per_sm >= 1 ? 1 : -1;
+  }
+  return cached[dev] > 0;
+}
+
+// The kernel waits at a grid barrier, so it is launched cooperatively: the
+// runtime starts it only with every CTA resident (while kernels on other
+// streams hold SMs it waits for them instead of starting part of the grid),
+// and refuses a grid that could never be co-resident; that refusal, or an
+// occupancy check that fails, sends the call to the multi-kernel path.
 template <int kMode>
 static int launch_fused_t(const FusedParams& p, int grid, cudaStream_t stream) {
   {
     const int rc = ep_host::ensure_max_smem(reinterpret_cast<const void*>(k_ll_fused<kMode>), (int)kFusedSmemCap);
     if (rc != EP_OK) return rc;
   }
-  k_ll_fused<kMode><<<grid, kFusedWarps * kWarp, fused_smem(p), stream>>>(p);
+  if (grid > ep_host::num_sms() || !fused_fits_one_per_sm<kMode>()) return kFusedNotLaunched;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kFusedWarps * kWarp);
+  cfg.dynamicSmemBytes = fused_smem(p);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_ll_fused<kMode>, p);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return kFusedNotLaunched;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return EP_ERR_CUDA;
+  }
   ep_host::count_launch();
-  return ep_host::check_launch();
+  return EP_OK;
 }
 
 static int launch_fused(const FusedParams& p, int fp8_mode, int grid, cudaStream_t stream) {
@@ -624,8 +680,10 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
     fp.ctl = static_cast<uint32_t*>(workspace);
     fp.status = status;
     fp.fp8 = fp8;
-    if (ep::plan_fused(fp, grid))
-      return ep::launch_fused(fp, fp8_mode, grid, s);
+    if (ep::plan_fused(fp, grid)) {
+      rc = ep::launch_fused(fp, fp8_mode, grid, s);
+      if (rc != ep::kFusedNotLaunched) return rc;
+    }
   }
 
   // larger batches: multi-CTA look-back layout; the scatter follows as its

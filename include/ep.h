@@ -117,7 +117,12 @@ int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E
  *    (stream-ordered); calls that overlap on the GPU race, so order them on
  *    one stream.
  *  - The first call on a device looks up the array's address with that
- *    device current; make it before any stream capture begins. */
+ *    device current; make it before any stream capture begins.  The address
+ *    is kept until the process exits: do not use the library on a device
+ *    after cudaDeviceReset on it.
+ *  - `stream` must belong to the current device (NULL: the current
+ *    device's default stream); a stream of another device returns
+ *    EP_ERR_INVALID_ARG, launching nothing. */
 int ep_get_dispatch_layout_no_alloc(const int64_t* topk_idx, int R, int T_r, int k, int E,
                                     int32_t* num_tokens_per_rank, int32_t* num_tokens_per_expert,
                                     uint8_t* is_token_in_rank, int32_t* slot_rank,

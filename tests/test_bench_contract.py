@@ -23,7 +23,10 @@ def test_reference_arm_prints_one_complete_line():
     assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 0
     assert d["higher_is_better"] is True and d["scaling"] == "weak"
     assert d["vs_baseline"] is None and d["data"] == "synthetic" and d["dtype"]
-    assert d["config"]["workload"].startswith("decode:")
+    assert d["config"]["workload"].startswith("large:")
+    import bench
+    from combine_get_dispatch_gb300 import synth
+    assert d["config"] == bench.config_of(synth.WORKLOADS["large"], 1)   # the GPU arm's config
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "tokens/s"
     assert cb["value"] == d["value"] and cb["sample"]
@@ -54,32 +57,39 @@ def test_gpu_arm_line_from_measurements():
         return r
 
     dec = synth.WORKLOADS["decode"]
-    pre = synth.WORKLOADS["prefill"]
-    e2e = {"ms": 0.2, "serial_ms": 0.34, "h2d_bytes_per_step": 29556736,
-           "d2h_bytes_per_step": 29360128}
+    lrg = synth.WORKLOADS["large"]
+    e2e = {"ms": 19.0, "serial_ms": 25.0, "h2d_bytes_per_step": 1891631104,
+           "d2h_bytes_per_step": 1879048192}
     results = {
+        "large": (lrg, SimpleNamespace(ll=False, rank=False),
+                  measured(lrg, lrg.T * lrg.k, 1.63, 2.45, 4.13, e2e)),
         "decode": (dec, SimpleNamespace(ll=True, rank=False),
-                   measured(dec, dec.T * dec.k, 0.032, 0.049, 0.081, e2e)),
-        "prefill": (pre, SimpleNamespace(ll=False, rank=False),
-                    measured(pre, pre.T * pre.k, 0.73, 0.62, 1.37)),
+                   measured(dec, dec.T * dec.k, 0.032, 0.049, 0.081)),
     }
     args = bench.parse_args(["--steps", "20", "--warmup", "5"])
     clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
-    line = bench.assemble_line(args, 1, "decode", results, clocks, 6750.0, "measured")
+    line = bench.assemble_line(args, 1, "large", results, clocks, 6750.0, "measured")
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "e2e", "clocks", "gpu_launches"):
         assert key in line, key
-    assert line["value"] == pytest.approx(dec.T / 0.081e-3) and line["ms_per_step"] == 0.081
+    assert line["value"] == pytest.approx(lrg.T / 4.13e-3) and line["ms_per_step"] == 4.13
     assert (line["n_gpus"], line["steps"], line["warmup"]) == (1, 20, 5)
-    assert line["config"]["workload"].startswith("decode:") and "l2" in line["config"]
+    assert line["config"]["workload"].startswith("large:") and "l2" in line["config"]
     rf = line["roofline"]
     assert rf["kernel"] == "k_combine" and rf["bound"] == "hbm" and rf["unit"] == "GB/s"
     assert rf["peak"] == 6750.0 and abs(rf["frac"] - rf["achieved"] / 6750.0) < 1e-3
-    assert abs(rf["achieved"] - results["decode"][2]["combine_gbs"]) < 0.1
+    assert abs(rf["achieved"] - results["large"][2]["combine_gbs"]) < 0.1
+    # the large combine moves 15.03 GB of rows in and 1.88 GB out per launch
+    assert rf["alg_bytes_per_launch"] == lrg.T * lrg.k * 2 * lrg.H + lrg.T * 2 * lrg.H
     assert rf["traffic"] is None or rf["traffic"] > 0
-    assert line["e2e"]["value"] == pytest.approx(dec.T / 0.2e-3)
-    assert line["e2e"]["h2d_bytes_per_step"] == 29556736
+    assert line["e2e"]["value"] == pytest.approx(lrg.T / 19.0e-3)
+    assert line["e2e"]["h2d_bytes_per_step"] == 1891631104
     assert line["clocks"] == clocks and line["gpu_launches"] == 40
-    assert set(line["workloads"]) == {"prefill"}
-    assert line["workloads"]["prefill"]["tokens_per_s"] == pytest.approx(pre.T / 1.37e-3)
+    assert set(line["workloads"]) == {"decode"}
+    wd = line["workloads"]["decode"]
+    assert wd["tokens_per_s"] == pytest.approx(dec.T / 0.081e-3)
+    # every other workload carries its own roofline object
+    rd = wd["roofline"]
+    assert rd["kernel"] == "k_combine" and rd["frac"] == pytest.approx(
+        results["decode"][2]["combine_gbs"] / 6750.0, abs=1e-3)

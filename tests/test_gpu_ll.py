@@ -221,3 +221,50 @@ def test_low_latency_dispatch_and_combine_replay_as_a_cuda_graph(fp8_mode):
         got = np_(out)
         want = oracle.combine(y_rows, wts, ref["combine_idx"], w.H)["out"]
         assert np.array_equal(got.reshape(want.shape), want)
+
+
+def _hold_lib(tmp_path):
+    """tests/cuda/hold_sms.cu built for this GPU (nvcc), loaded by ctypes."""
+    import ctypes
+    import os
+    import subprocess
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "cuda", "hold_sms.cu")
+    so = str(tmp_path / "libhold.so")
+    nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-shared",
+                        "-Xcompiler", "-fPIC", src, "-o", so], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lib = ctypes.CDLL(so)
+    lib.hold_sms.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p]
+    lib.hold_sms.restype = ctypes.c_int
+    return lib
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("held", ["half", "all"])
+def test_ll_dispatch_while_another_stream_holds_sms(tmp_path, held):
+    """The single-launch decode kernel waits at a grid barrier, so its CTAs
+    must all be resident together.  Here another stream holds half, or all,
+    of the SMs for 20 ms (each holding CTA takes 120 KB of shared memory, so
+    a dispatch CTA cannot share its SM) while ep_ll_dispatch is issued: the
+    call must still return the oracle's results with status EP_OK (the
+    kernel starts once its whole grid fits, or the call takes the
+    multi-kernel path), not a timed-out barrier."""
+    lib = _hold_lib(tmp_path)
+    w = synth.WORKLOADS["decode"]
+    x_dev, x_host, idx_dev, idx, _, _ = inputs(w)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ws = ep.alloc_workspace(w.R, w.T_r, w.k, w.E, w.H)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    ctas = sms // 2 if held == "half" else sms
+    assert lib.hold_sms(ctas, 120 * 1024, 20_000_000, ctypes_stream(side)) == 0
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, w.fp8_mode, ws=ws)
+    torch.cuda.synchronize()
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    _compare_ll(w, x_host, idx, d, w.max_tokens_per_rank, w.fp8_mode)
+
+
+def ctypes_stream(s):
+    import ctypes
+    return ctypes.c_void_p(s.cuda_stream)
