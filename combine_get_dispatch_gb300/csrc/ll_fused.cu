@@ -60,6 +60,7 @@ constexpr int kFusedMaxIds = 4 * kFusedWarps * kWarp * kScanIdsPerThread;   // a
 constexpr int kFusedBarBytes = 2 * kFusedWarps * kFusedMaxPerWarp * 8;   // load + quantised barriers
 constexpr size_t kFusedSmemCap = 225 * 1024;
 static_assert(kRankWarps == kFusedWarps - kQuantWarps, "FP8: the rank warps are the store warps");
+static_assert(kFusedMaxPerWarp <= kWarp, "a warp issues its pieces one per lane");
 constexpr int kCtlArrive = 8;            // workspace control words of this kernel
 constexpr int kCtlExit = 9;
 
@@ -212,9 +213,10 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   const int grid = (int)gridDim.x;
   const int cta = (int)blockIdx.x;
 
-  const int32_t U = p.n_units;
-  const int32_t u0 = (int32_t)((int64_t)U * cta / grid);
-  const int32_t u1 = (int32_t)((int64_t)U * (cta + 1) / grid);
+  // U * grid < 2^32 (checked on the host): 32-bit unit range arithmetic
+  const uint32_t U = (uint32_t)p.n_units;
+  const int32_t u0 = (int32_t)(U * (uint32_t)cta / (uint32_t)grid);
+  const int32_t u1 = (int32_t)(U * (uint32_t)(cta + 1) / (uint32_t)grid);
   // FP8: warps 0..kQuantWarps-1 own (load, quantise) the units, the rest
   // issue their bulk stores; bf16: every warp owns units and stores them
   constexpr int kOwnWarps = kFp8 ? kQuantWarps : kFusedWarps;
@@ -273,8 +275,8 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
     tma_load_1d_hint(unit_slot(m), p.x + (int64_t)g * p.H * 2 + (int64_t)pc * p.Hp * 2, bytes, &bars[m],
                      l2_policy_evict_first());   // every token is read once
   };
-  if (kFp8 && tid == kThreads - 1) {
-    for (int32_t q = 0; q < u1 - u0; ++q) mbar_init(&qbars[q], 1);
+  if (kFp8 && warp == kFusedWarps - 1) {   // the quantised-unit barriers, a lane each
+    for (int32_t q = lane; q < u1 - u0; q += kWarp) mbar_init(&qbars[q], 1);
     fence_barrier_init();
   }
   if (nm > 0 && lane == 0) {
@@ -287,9 +289,10 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
   __syncthreads();
   // every thread's id loads are issued now: the rest of the pieces queue
   // behind them (issued any earlier, a piece could go out ahead of another
-  // thread's ids and hold them back), landing while the ids are counted
-  if (nm > 0 && lane == 0)
-    for (int32_t m = min(nm, kEarlyUnits); m < nm; ++m) load_unit(m);
+  // thread's ids and hold them back), landing while the ids are counted.
+  // Lane m issues the warp's piece m: one thread's bulk copies are issued
+  // one after another.
+  if (lane >= min(nm, kEarlyUnits) && lane < nm) load_unit(lane);
 
   // ---- 1. per-expert counts of the ids before the own range, and the own ids
   {
@@ -535,6 +538,8 @@ static size_t fused_smem(const FusedParams& p) {
 // Geometry of the fused path, or false when the batch does not fit it.
 static bool plan_fused(FusedParams& p, int grid) {
   if ((int64_t)p.T * p.k > kFusedMaxIds || p.T == 0) return false;
+  if ((int64_t)p.T * ((p.H + kFusedPiece - 1) / kFusedPiece) * grid >= ((int64_t)1 << 32))
+    return false;   // the kernel's unit-range arithmetic is 32-bit
   const int hp = std::min(p.H, kFusedPiece);
   p.Hp = hp;
   p.P = (p.H + hp - 1) / hp;
