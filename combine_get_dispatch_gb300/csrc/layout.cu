@@ -33,7 +33,9 @@
 
 namespace ep {
 
-constexpr int kIdsPerLane = 4;            // ids per thread per chunk
+constexpr int kIdsPerLane = 4;            // ids per thread per chunk (low latency; normal mode up
+                                          // to one wave of chunks, see launch_layout)
+constexpr int kMaxIdsPerLane = 16;        // normal mode, batches of more than a wave of chunks
 constexpr int kLookbackWindow = 16;
 constexpr int kSmallLLThreads = 256;       // low-latency batches up to kSmallLLMaxIds
 constexpr int64_t kSmallLLMaxIds = 32768;
@@ -71,59 +73,81 @@ __device__ __forceinline__ uint64_t wait_flag(const uint64_t* addr, uint64_t f, 
   return pack_flag(epoch, kFlagAggregate, 0);
 }
 
-template <bool kLL, int kLayoutThreads>
+// The rank of expert e (e / E_l) by a multiply with el_magic = floor(2^32 /
+// E_l) + 1, exact for 0 <= e < 2^32 / E_l (E_l <= 1024, e < 1024 here).
+__device__ __forceinline__ int rank_of(int e, const LayoutParams& p) {
+  return (int)(((uint64_t)(uint32_t)e * p.el_magic) >> 32);
+}
+
+// Transpose of a 32 x 32 bit matrix held one row per lane (lane i, bit j =
+// entry (i, j)): on return lane j holds column j (bit i = entry (i, j)).
+// Five exchange rounds, swapping the off-diagonal blocks of 16, 8, 4, 2 and
+// 1 bits with the partner lane.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+  constexpr uint32_t kLeft[5] = {0x0000ffffu, 0x00ff00ffu, 0x0f0f0f0fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    const int j = 16 >> r;
+    const uint32_t m = kLeft[r];   // columns whose index has bit j clear
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+    x = (lane & j) ? ((x & ~m) | ((y & ~m) >> j)) : ((x & m) | ((y & m) << j));
+  }
+  return x;
+}
+
+template <bool kLL, int kLayoutThreads, int kIds>
 __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
   constexpr int kLayoutWarps = kLayoutThreads / kWarp;
-  constexpr int kMaxChunkIds = kLayoutThreads * kIdsPerLane;
-  extern __shared__ int32_t smem[];
+  constexpr int kMaxChunkIds = kLayoutThreads * kIds;
+  static_assert(kMaxChunkIds % 2 == 0 && kLayoutWarps % 2 == 0, "s_mask must stay 8-byte aligned");
+  extern __shared__ __align__(16) int32_t smem[];
   int32_t* s_ids = smem;                                  // [kMaxChunkIds]
   int32_t* s_cnt = s_ids + kMaxChunkIds;                  // [warps][E]
   int32_t* s_agg = s_cnt + kLayoutWarps * p.E;            // [V]
   int32_t* s_excl = s_agg + p.V;                          // [V]
+  uint64_t* s_mask = reinterpret_cast<uint64_t*>(s_excl + p.V);   // [chunk_tokens] (8-byte aligned:
+                                                                   // every count above is even)
   __shared__ uint32_t s_ticket, s_epoch;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int nbits = key_bits(p.E);
+  // normal mode with one chunk per rank: no chunk waits for another, so the
+  // CTA index is the chunk (no ticket) and no look-back word is published
+  const bool solo = !kLL && p.chunks_per_rank == 1;
 
   if (kLL || p.trigger_dependents) pdl_launch_dependents();   // the scatter may start loading x
-  if (tid == 0) {
+  if (tid == 0 && !solo) {
     s_ticket = atomicAdd(&p.ctl[0], 1u);
     s_epoch = ld_relaxed_u32(&p.ctl[2]);
   }
   for (int v = tid; v < kLayoutWarps * p.E; v += kLayoutThreads) s_cnt[v] = 0;
   for (int v = p.E + tid; v < p.V; v += kLayoutThreads) s_agg[v] = 0;
-  __syncthreads();
 
-  const uint32_t b = s_ticket;
-  const uint32_t epoch = s_epoch & 0x3fffffffu;
-  if (b >= (uint32_t)p.num_chunks) {   // workspace not cleaned: give up loudly
-    if (tid == 0) {
-      atomicExch(&p.ctl[3], 1u);
-      set_status(p.status, EP_ERR_STATE);
-    }
-    return;
-  }
-  const int i = (int)b / p.chunks_per_rank;
-  const int c = (int)b % p.chunks_per_rank;
-  const int t0 = c * p.chunk_tokens;
-  const int nt = max(0, min(p.chunk_tokens, p.T_r - t0));
-  const int n = nt * p.k;
-  const int64_t id_base = ((int64_t)i * p.T_r + t0) * p.k;
-
+  // chunk b: source rank i, tokens [t0, t0 + nt), ids [id_base, id_base + n)
+  int i = 0, c = 0, t0 = 0, nt = 0, n = 0;
+  int64_t id_base = 0;
+  auto chunk_of = [&](uint32_t bb) {
+    i = (int)bb / p.chunks_per_rank;
+    c = (int)bb % p.chunks_per_rank;
+    t0 = c * p.chunk_tokens;
+    nt = max(0, min(p.chunk_tokens, p.T_r - t0));
+    n = nt * p.k;
+    id_base = ((int64_t)i * p.T_r + t0) * p.k;
+  };
   // ---- 1. load the chunk's ids (validated) into shared memory; all loads
   //      of a thread are issued before the first is used
-  {
-    int64_t ev[kIdsPerLane];
+  auto load_ids = [&]() {
+    int64_t ev[kIds];
 #pragma unroll
-    for (int u = 0; u < kIdsPerLane; ++u) {
+    for (int u = 0; u < kIds; ++u) {
       const int q = tid + u * kLayoutThreads;
       ev[u] = q < n ? __ldg(&p.topk_idx[id_base + q]) : -1;
     }
     bool bad = false;
 #pragma unroll
-    for (int u = 0; u < kIdsPerLane; ++u) {
+    for (int u = 0; u < kIds; ++u) {
       const int q = tid + u * kLayoutThreads;
       if (q < n) {
         const int64_t e = ev[u];
@@ -134,15 +158,36 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
       }
     }
     if (bad) set_status(p.status, EP_ERR_INVALID_ARG);
+  };
+
+  uint32_t b = blockIdx.x;
+  uint32_t epoch = 0;
+  if (solo) {   // the ids go out at once, ahead of the barrier
+    chunk_of(b);
+    load_ids();
+    __syncthreads();
+  } else {
+    __syncthreads();
+    b = s_ticket;
+    epoch = s_epoch & 0x3fffffffu;
+    if (b >= (uint32_t)p.num_chunks) {   // workspace not cleaned: give up loudly
+      if (tid == 0) {
+        atomicExch(&p.ctl[3], 1u);
+        set_status(p.status, EP_ERR_STATE);
+      }
+      return;
+    }
+    chunk_of(b);
+    load_ids();
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- per-warp ranks: warp w owns a contiguous run of the chunk's ids
   const int per_warp = ((n + kLayoutThreads - 1) / kLayoutThreads) * kWarp;
   const int wbase = warp * per_warp;
-  int my_rank[kIdsPerLane];
+  int my_rank[kIds];
 #pragma unroll
-  for (int u = 0; u < kIdsPerLane; ++u) {
+  for (int u = 0; u < kIds; ++u) {
     my_rank[u] = 0;
     if (u * kWarp < per_warp) {
       const int q = wbase + u * kWarp + lane;
@@ -170,13 +215,36 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
     s_agg[e] = run;
   }
   // ---- normal mode: is_token_in_rank and tokens per destination rank
-  if (!kLL) {
+  if (!kLL && p.R <= 64) {
+    // each token's destination ranks as a bit mask; the tokens per rank from
+    // a bit transpose over 32 tokens at a time (a hot rank gets one shared
+    // atomic per warp, not one per token); the chunk's is_token_in_rank rows
+    // are one contiguous byte range, written with 16-byte stores below
+    for (int base = warp * kWarp; base < nt; base += kLayoutThreads) {
+      const int tt = base + lane;
+      uint64_t m = 0;
+      if (tt < nt) {
+        for (int j = 0; j < p.k; ++j) {
+          const int e = s_ids[tt * p.k + j];
+          if (e >= 0) m |= 1ull << rank_of(e, p);
+        }
+        s_mask[tt] = m;
+      }
+      // lane r's column of the warp's 32 x R bit matrix: its tokens for rank r
+      const uint32_t lo = transpose32((uint32_t)m, lane);
+      if (lane < p.R && lo != 0u) atomicAdd(&s_agg[p.E + lane], __popc(lo));
+      if (p.R > 32) {
+        const uint32_t hi = transpose32((uint32_t)(m >> 32), lane);
+        if (lane + 32 < p.R && hi != 0u) atomicAdd(&s_agg[p.E + 32 + lane], __popc(hi));
+      }
+    }
+  } else if (!kLL) {
     for (int tt = tid; tt < nt; tt += kLayoutThreads) {
       const int32_t* te = s_ids + tt * p.k;
       uint8_t* row = p.is_token_in_rank + ((int64_t)i * p.T_r + t0 + tt) * p.R;
       int dst[kMaxK];
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) dst[j] = (j < p.k && te[j] >= 0) ? te[j] / p.E_l : -1;
+      for (int j = 0; j < kMaxK; ++j) dst[j] = (j < p.k && te[j] >= 0) ? rank_of(te[j], p) : -1;
       for (int r = 0; r < p.R; ++r) {
         bool hit = false;
 #pragma unroll
@@ -188,10 +256,41 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
   }
   __syncthreads();
 
+  if (!kLL && p.R <= 64) {
+    // is_token_in_rank rows [i][t0, t0 + nt): byte q is token q / R, rank q % R
+    uint8_t* out = p.is_token_in_rank + ((int64_t)i * p.T_r + t0) * p.R;
+    const int nbytes = nt * p.R;
+    const int head = min(nbytes, (int)((16u - (uint32_t)(reinterpret_cast<uintptr_t>(out) & 15u)) & 15u));
+    const int nbody = (nbytes - head) / 16;
+    auto byte_at = [&](int q) -> uint32_t {
+      const int tq = q / p.R;
+      return (uint32_t)((s_mask[tq] >> (q - tq * p.R)) & 1ull);
+    };
+    if (tid < head) out[tid] = (uint8_t)byte_at(tid);
+    for (int g = tid; g < nbody; g += kLayoutThreads) {
+      const int q0 = head + g * 16;
+      int tq = q0 / p.R;
+      int r = q0 - tq * p.R;
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        w[u >> 2] |= (uint32_t)((s_mask[tq] >> r) & 1ull) << (8 * (u & 3));
+        if (++r == p.R) {
+          r = 0;
+          ++tq;
+        }
+      }
+      st_v4(out + q0, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+    for (int q = head + nbody * 16 + tid; q < nbytes; q += kLayoutThreads) out[q] = (uint8_t)byte_at(q);
+  }
+
   // ---- 2. publish the aggregate, look back for the exclusive prefix
   const int seq_first = kLL ? 0 : i * p.chunks_per_rank;
   uint64_t* F = p.flags;
-  if ((int)b == seq_first) {
+  if (solo) {   // a chunk per rank: its prefix within the rank is 0, nobody reads its words
+    for (int v = tid; v < p.V; v += kLayoutThreads) s_excl[v] = 0;
+  } else if ((int)b == seq_first) {
     for (int v = tid; v < p.V; v += kLayoutThreads) {
       s_excl[v] = 0;
       st_relaxed_u64(&F[(size_t)b * p.V + v], pack_flag(epoch, kFlagInclusive, (uint32_t)s_agg[v]));
@@ -229,7 +328,7 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
 
   // ---- 3. per-slot outputs
 #pragma unroll
-  for (int u = 0; u < kIdsPerLane; ++u) {
+  for (int u = 0; u < kIds; ++u) {
     if (u * kWarp < per_warp) {
       const int q = wbase + u * kWarp + lane;
       if (q < n) {
@@ -296,11 +395,12 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
   if (tid == 0) {
     if (p.fuse_notify) __threadfence();   // this CTA's count rows, before the arrival
     const uint32_t d = atomicAdd(&p.ctl[1], 1u);
+    if (d >= (uint32_t)p.num_chunks) set_status(p.status, EP_ERR_STATE);   // not cleaned
     const bool last = d == (uint32_t)p.num_chunks - 1;
     if (last) {
       p.ctl[0] = 0;
       p.ctl[1] = 0;
-      p.ctl[2] = s_epoch + 1;
+      p.ctl[2] = ld_relaxed_u32(&p.ctl[2]) + 1;   // the next launch's epoch
       p.ctl[3] = 0;
       if (p.fuse_notify) __threadfence();   // ... and everyone else's, before the reads
     }
@@ -308,7 +408,11 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
   }
   if (!kLL && p.fuse_notify) {
     __syncthreads();
-    if (s_last) notify_tables<true>(p.nt, tid, kLayoutThreads, smem);   // smem is free now
+    if (s_last) {   // smem is free now: aligned totals, then (if they fit) the staged counts
+      const int e4 = (p.E + 3) & ~3;
+      const bool staged = notify_stage_words(p.R, p.E) <= kNotifyStageMaxWords;
+      notify_tables<true>(p.nt, tid, kLayoutThreads, smem, staged ? smem + e4 : nullptr);
+    }
   }
 }
 
@@ -337,10 +441,11 @@ size_t layout_region_bytes(int R, int T_r, int k, int E) {
   return b;
 }
 
-template <bool kLL, int kThreads>
+template <bool kLL, int kThreads, int kIds>
 static int launch_layout_t(LayoutParams p, void* ws, cudaStream_t stream) {
   char* base = static_cast<char*>(ws);
-  const LayoutGeometry g = layout_geometry(p.R, p.T_r, p.k, p.E, kThreads * kIdsPerLane);
+  const LayoutGeometry g = layout_geometry(p.R, p.T_r, p.k, p.E, kThreads * kIds);
+  p.el_magic = (uint64_t)((1ull << 32) / (uint64_t)p.E_l) + 1;
   p.ctl = reinterpret_cast<uint32_t*>(base);
   p.flags = reinterpret_cast<uint64_t*>(base + g.flags_offset);
   p.rank_start = reinterpret_cast<uint64_t*>(base + g.rank_start_offset);
@@ -348,24 +453,43 @@ static int launch_layout_t(LayoutParams p, void* ws, cudaStream_t stream) {
   p.chunks_per_rank = g.chunks_per_rank;
   p.num_chunks = (int)g.num_chunks;
   p.V = kLL ? p.E : p.E + p.R;
-  auto smem_bytes = [](int E, int V) {
-    return sizeof(int32_t) * ((size_t)kThreads * kIdsPerLane + (size_t)(kThreads / kWarp) * E + 2 * (size_t)V);
+  // ids, per-warp counts, aggregates and prefixes, the token masks (normal
+  // mode); the last CTA reuses it for the notify tables (normal mode, fused)
+  auto smem_bytes = [](int E, int V, int chunk_tokens, int R, bool notify) {
+    const size_t words = (size_t)kThreads * kIds + (size_t)(kThreads / kWarp) * E + 2 * (size_t)V;
+    size_t b = sizeof(int32_t) * words + (kLL ? 0 : sizeof(uint64_t) * (size_t)chunk_tokens);
+    const int64_t stage = notify_stage_words(R, E);
+    if (notify && stage <= kNotifyStageMaxWords)
+      b = std::max(b, sizeof(int32_t) * ((size_t)((E + 3) & ~3) + (size_t)stage));
+    return b;
   };
   {
-    const int rc = ep_host::ensure_max_smem(reinterpret_cast<const void*>(k_layout<kLL, kThreads>), (int)smem_bytes(kMaxE, kMaxE + kMaxR));
+    const size_t cap = std::max(smem_bytes(kMaxE, kMaxE + kMaxR, kThreads * kIds, 1, false),
+                                sizeof(int32_t) * ((size_t)kMaxE + kNotifyStageMaxWords));
+    const int rc = ep_host::ensure_max_smem(reinterpret_cast<const void*>(k_layout<kLL, kThreads, kIds>), (int)cap);
     if (rc != EP_OK) return rc;
   }
-  k_layout<kLL, kThreads><<<p.num_chunks, kThreads, smem_bytes(p.E, p.V), stream>>>(p);
+  k_layout<kLL, kThreads, kIds><<<p.num_chunks, kThreads,
+                            smem_bytes(p.E, p.V, p.chunk_tokens, p.R, !kLL && p.fuse_notify), stream>>>(p);
   ep_host::count_launch();
   return ep_host::check_launch();
 }
 
 int launch_layout(const LayoutParams& p, bool ll, void* ws, cudaStream_t stream) {
-  if (!ll) return launch_layout_t<false, kNormalChunkIds / kIdsPerLane>(p, ws, stream);
+  constexpr int kThreads = kNormalChunkIds / kIdsPerLane;
+  if (!ll) {
+    // normal mode: chunks of 2048 ids while they fit in one wave (a CTA per
+    // SM), else 8192 ids per chunk -- fewer, longer CTAs and a shorter
+    // look-back chain instead of several waves of latency-bound ones
+    const int64_t ids = (int64_t)p.R * p.T_r * p.k;
+    if (ids <= (int64_t)ep_host::num_sms() * kNormalChunkIds)
+      return launch_layout_t<false, kThreads, kIdsPerLane>(p, ws, stream);
+    return launch_layout_t<false, kThreads, kMaxIdsPerLane>(p, ws, stream);
+  }
   // decode-sized batches: smaller CTAs (they fit beside the scatter CTAs
   // that follow as a programmatic dependent launch), 1024 ids per chunk
-  if (small_ll(p.R, p.T_r, p.k)) return launch_layout_t<true, kSmallLLThreads>(p, ws, stream);
-  return launch_layout_t<true, kNormalChunkIds / kIdsPerLane>(p, ws, stream);
+  if (small_ll(p.R, p.T_r, p.k)) return launch_layout_t<true, kSmallLLThreads, kIdsPerLane>(p, ws, stream);
+  return launch_layout_t<true, kThreads, kIdsPerLane>(p, ws, stream);
 }
 
 }  // namespace ep

@@ -12,6 +12,7 @@ namespace ep {
 struct LayoutParams {
   const int64_t* topk_idx;
   int R, T_r, k, E, E_l;
+  uint64_t el_magic;   // floor(2^32 / E_l) + 1: rank of an expert by a multiply
   int chunk_tokens, chunks_per_rank, num_chunks, V;
   // normal-mode outputs (get_dispatch_layout)
   int32_t* num_tokens_per_rank;
@@ -44,7 +45,8 @@ struct LayoutGeometry {
   size_t flags_offset, rank_start_offset, bytes;
 };
 
-constexpr int kNormalChunkIds = 2048;   // ids per chunk (512 threads x 4)
+constexpr int kNormalChunkIds = 2048;   // ids per chunk (512 threads x 4); the layout's workspace
+                                        // is sized for it (larger chunks need less)
 
 LayoutGeometry layout_geometry(int R, int T_r, int k, int E, int chunk_ids);
 

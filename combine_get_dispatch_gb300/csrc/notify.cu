@@ -23,9 +23,12 @@ namespace ep {
 
 constexpr int kNotifyThreads = 1024;
 
-__global__ void __launch_bounds__(kNotifyThreads) k_notify(NotifyParams p) {
+// staged: the count tables are loaded into dynamic shared memory first
+// (notify_stage_words(R, E) words), see notify_tables.
+__global__ void __launch_bounds__(kNotifyThreads) k_notify(NotifyParams p, int staged) {
   __shared__ int32_t s_recv[kMaxE];
-  notify_tables<false>(p, threadIdx.x, kNotifyThreads, s_recv);
+  extern __shared__ __align__(16) int32_t s_stage[];
+  notify_tables<false>(p, threadIdx.x, kNotifyThreads, s_recv, staged ? s_stage : nullptr);
 }
 
 }  // namespace ep
@@ -86,7 +89,15 @@ extern "C" int ep_notify_dispatch(const int32_t* num_tokens_per_rank,
     for (int r = 0; r < R; ++r) h[r] = -1;
     p.host_recv_rows = static_cast<int64_t*>(dev);
   }
-  ep::k_notify<<<1, ep::kNotifyThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  const int64_t words = ep::notify_stage_words(R, E);
+  const bool staged = words <= ep::kNotifyStageMaxWords;
+  {
+    const int rc = ep_host::ensure_max_smem(reinterpret_cast<const void*>(ep::k_notify),
+                                            ep::kNotifyStageMaxWords * (int)sizeof(int32_t));
+    if (rc != EP_OK) return rc;
+  }
+  ep::k_notify<<<1, ep::kNotifyThreads, staged ? (size_t)words * sizeof(int32_t) : 0,
+                 static_cast<cudaStream_t>(stream)>>>(p, staged ? 1 : 0);
   ep_host::count_launch();
   int rc = ep_host::check_launch();
   if (rc != EP_OK || !wait) return rc;

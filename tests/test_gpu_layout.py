@@ -53,6 +53,12 @@ def test_layout_and_notify_full_size(name):
     (1, 5000, 16, 32),   # k = 16 (chunks of 128 tokens), one rank
     (64, 40, 4, 256),    # many ranks
     (2, 3000, 8, 1024),  # largest expert count
+    (3, 700, 3, 6),      # odd E + R (shared-memory tables of odd length)
+    (33, 100, 5, 66),    # R not a power of two, odd E + R
+    (100, 30, 4, 200),   # R > 64: per-rank loop for is_token_in_rank; counts walked in memory
+    (96, 12, 2, 192),    # R > 64, notify counts too large to stage
+    (3, 110000, 1, 9),   # beyond one wave of 2048-id chunks: 8192-id chunks (k = 1), ragged
+    (2, 20000, 8, 64),   # 8192-id chunks at k = 8, look-back over 19 chunks
 ])
 def test_layout_edge_shapes(R, T_r, k, E):
     rng = np.random.default_rng(R * 1000 + T_r)

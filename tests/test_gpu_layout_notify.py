@@ -66,8 +66,14 @@ def test_fused_layout_notify_full_size(name):
     (3, 1, 1, 3, 4),        # one token
     (2, 257, 8, 64, 128),   # ragged chunk tail
     (1, 5000, 16, 32, 1),   # one rank, k = 16
-    (64, 40, 4, 256, 8),    # many ranks
+    (64, 40, 4, 256, 8),    # many ranks (64: the largest bit-mask case), counts staged
     (2, 3000, 8, 1024, 1),  # largest expert count
+    (3, 700, 3, 6, 4),      # odd E + R
+    (33, 100, 5, 66, 1),    # one chunk per rank, R not a power of two
+    (100, 30, 4, 200, 1),   # R > 64 (per-rank loop for is_token_in_rank), counts walked
+    (128, 20, 3, 256, 16),  # counts too large to stage: the last CTA walks them in memory
+    (8, 2500, 8, 256, 1),   # several chunks per rank (look-back), counts staged
+    (4, 40000, 2, 128, 4),  # beyond one wave of 2048-id chunks: 8192-id chunks, ragged
 ])
 def test_fused_layout_notify_edge_shapes(R, T_r, k, E, A):
     rng = np.random.default_rng(R * 1000 + T_r + 7)
