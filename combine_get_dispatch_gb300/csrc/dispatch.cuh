@@ -52,8 +52,13 @@ __host__ __device__ inline int scale_row_bytes(int H, int elem) {
   return ((H / kFp8Block) * elem + 15) / 16 * 16;
 }
 
+constexpr float kFloatMax = 3.40282346638528859812e+38f;   // largest finite float
+
 // Quantise 16 channels (two 16-byte bf16 vectors) of this lane; amax is
-// reduced over the 8 lanes sharing the 128-channel block.  Returns 16 E4M3
+// reduced over the 8 lanes sharing the 128-channel block (NaN entries do not
+// raise it), floored at 1e-4 and capped at the largest finite float, so a
+// block holding an infinity still gets a finite scale and the infinity
+// saturates to +-448.  Returns 16 E4M3
 // bytes; the block's scale goes to *sf (fp32 mode) or *su (ue8m0 mode).
 template <int kMode>
 __device__ __forceinline__ uint4 quantize16(const uint4 a, const uint4 b, float* sf, uint32_t* su) {
@@ -69,7 +74,7 @@ __device__ __forceinline__ uint4 quantize16(const uint4 a, const uint4 b, float*
   for (int c = 0; c < 16; ++c) amax = fmaxf(amax, fabsf(f[c]));
 #pragma unroll
   for (int off = 4; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  amax = fmaxf(amax, 1e-4f);
+  amax = fminf(fmaxf(amax, 1e-4f), kFloatMax);   // floor; an infinity saturates
   float mul;
   if (kMode == EP_FP8_E4M3_F32_SCALE) {
     *sf = __fdiv_rn(amax, 448.0f);

@@ -32,7 +32,8 @@
  * Readings where the article is silent (each also listed in the design
  * notes): rows of a segment are ordered by (source rank, token, slot);
  * topk id -1 means "no expert"; FP8 blocks are 128 channels; amax is floored
- * at 1e-4; fp32 mode stores scale = amax/448 and quantises x * (448/amax);
+ * at 1e-4 and capped at the largest finite float (an infinity in x gives a
+ * finite scale; the infinity itself saturates to +-448); fp32 mode stores scale = amax/448 and quantises x * (448/amax);
  * ue8m0 mode rounds amax/448 up to a power of two and stores its biased
  * exponent byte; combine accumulates w*y in fp32 with fma in slot order and
  * rounds once to bf16.
@@ -40,6 +41,7 @@
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared (no fast-math, no
  * contraction: every float operation below is one IEEE-754 rounding).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -137,7 +139,9 @@ void ep_oracle_e4m3_to_f32_batch(const uint8_t* in, int64_t n, float* out) {
 /* ------------------------------------------------------------------ */
 
 /* Quantise one bf16 row of H channels (H % 128 == 0) block by block.
- *   amax  = max(max |x| over the block, 1e-4)
+ *   amax  = min(max(max |x| over the block, 1e-4), FLT_MAX)
+ *           (NaN entries do not raise amax; an infinity saturates it to the
+ *           largest finite float, so every scale stays finite)
  *   mode 1 (fp32 scale): scale = amax / 448, q = E4M3(x * (448 / amax))
  *   mode 2 (ue8m0):      s = amax / 448 rounded UP to a power of two 2^p
  *                        (biased exponent + 1 when any mantissa bit is set),
@@ -157,6 +161,7 @@ void ep_oracle_quantize_row(const uint16_t* x, int H, int mode, uint8_t* q,
       if (a > amax) amax = a;
     }
     if (amax < 1e-4f) amax = 1e-4f;
+    if (amax > FLT_MAX) amax = FLT_MAX;   /* an infinity in the block saturates */
     if (mode == FP8_E4M3_F32_SCALE) {
       float scale = amax / 448.0f;
       float inv = 448.0f / amax;

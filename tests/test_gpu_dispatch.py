@@ -284,3 +284,72 @@ def test_fp32_scale_buffer_must_be_word_aligned():
     assert rc == ep.EP_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert int(status.item()) == ep.EP_OK
+
+
+def _e4m3_equal(got, want):
+    """E4M3 codes equal, a NaN code (S.1111.111) matching a NaN of either sign."""
+    got, want = got.view(np.uint8), want.view(np.uint8)
+    nan = (want & 0x7F) == 0x7F
+    return np.array_equal(got[~nan], want[~nan]) and np.all((got[nan] & 0x7F) == 0x7F)
+
+
+def _plant_non_finite(x_host):
+    x = x_host.copy()
+    x[0, 0, 5] = 0x7F80           # +inf in a block of finite values
+    x[1, 3, 130] = 0xFF80         # -inf
+    x[0, 1, :128] = 0x7F80        # a whole block of +inf
+    x[2, 7, 300] = 0x7FC0         # NaN among finite values
+    x[3, 15, 511] = 0xFFC1        # NaN with the sign bit set
+    x[3, 14, 384:512] = 0xFFC0    # a whole block of NaN (amax stays at the floor)
+    return x
+
+
+@pytest.mark.parametrize("fp8_mode", [1, 2])
+def test_dispatch_fp8_non_finite_inputs(fp8_mode):
+    """Blocks holding infinities or NaN: amax ignores NaN and saturates an
+    infinity to the largest finite float, so scales stay finite and match
+    the oracle bit for bit; every NaN input gives an E4M3 NaN code (its sign
+    is not specified)."""
+    w = synth.scaled(synth.WORKLOADS["tiny"], fp8_mode=fp8_mode, H=512)
+    _, x_host, idx_dev, idx, _, _ = inputs(w)
+    x_host = _plant_non_finite(x_host)
+    x_dev = to_dev_bf16(x_host)
+    lay = gpu_layout(idx_dev, w.E)
+    nt = gpu_notify(lay, w.E, 1)
+    _, _, ref, cap = oracle_normal(x_host, idx, w.E, 1, fp8_mode)
+    d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, fp8_mode, cap)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    src = np_(d["recv_src_idx"])
+    assert np.array_equal(src, ref["recv_src_idx"])
+    rows = np.nonzero(src.reshape(-1) >= 0)[0]
+    got = np_(d["recv_x"]).reshape(w.R * cap, -1)[rows]
+    want = ref["recv_x"].reshape(w.R * cap, -1)[rows]
+    assert _e4m3_equal(got, want)
+    r_idx, row_idx = np.divmod(rows, cap)
+    gs, rs = np_(d["recv_scales"]), ref["recv_scales"]
+    assert np.array_equal(gs[r_idx, :, row_idx], rs[r_idx, :, row_idx])
+    # the block of +inf: +448 codes
+    assert np.all(want.view(np.uint8).reshape(len(rows), -1)[src.reshape(-1)[rows] == 1, :128] == 0x7E)
+
+
+@pytest.mark.parametrize("fp8_mode", [1, 2])
+def test_ll_dispatch_fp8_non_finite_inputs(fp8_mode):
+    """The same non-finite inputs through the single-launch low-latency path."""
+    from ep_harness import gpu_ll_dispatch
+    w = synth.scaled(synth.WORKLOADS["tiny"], fp8_mode=fp8_mode, H=512)
+    _, x_host, idx_dev, idx, _, _ = inputs(w)
+    x_host = _plant_non_finite(x_host)
+    x_dev = to_dev_bf16(x_host)
+    d = gpu_ll_dispatch(x_dev, idx_dev, w.E, w.max_tokens_per_rank, fp8_mode)
+    assert ep.ep_read_status(d["status"]) == ep.EP_OK
+    ref = oracle.ll_dispatch(x_host, idx, w.E, w.max_tokens_per_rank, fp8_mode)
+    assert np.array_equal(np_(d["recv_count"]), ref["recv_count"])
+    S = w.R * w.max_tokens_per_rank
+    cnt = ref["recv_count"].reshape(-1)
+    px = np_(d["packed_recv_x"]).reshape(w.E, S, -1)
+    rpx = ref["packed_recv_x"].reshape(w.E, S, -1)
+    ps = np_(d["packed_recv_scales"]).reshape(w.E, w.H // 128, S)
+    rps = ref["packed_recv_scales"].reshape(w.E, w.H // 128, S)
+    for e in range(w.E):
+        assert _e4m3_equal(px[e, :cnt[e]], rpx[e, :cnt[e]]), e
+        assert np.array_equal(ps[e, :, :cnt[e]], rps[e, :, :cnt[e]]), e

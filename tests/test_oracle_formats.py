@@ -126,3 +126,40 @@ def test_all_zero_block_uses_floor():
     q, s = oracle.quantize_row(x, oracle.FP8_E4M3_UE8M0)
     # 1e-4 / 448 = 2.23e-7 rounds up to 2^-22 -> biased exponent 105
     assert np.all(q == 0) and np.all(s == 105)
+
+
+def test_quantise_block_holding_an_infinity_or_nan():
+    """Non-finite inputs (the article fixes nothing for them; reading: amax
+    ignores NaN and is capped at the largest finite float, so scales stay
+    finite).  Expected codes derived by hand: FLT_MAX/448 ~ 7.595e35 lies in
+    (2^119, 2^120], so the ue8m0 block with an infinity gets 2^120 (byte
+    127 + 120 = 247); +-inf saturate to +-448 (0x7E / 0xFE) and the finite
+    values, scaled by 2^-120, round to +-0 (0x00 / 0x80).  The NaN block's
+    amax is 3.0: 3/448 lies in (2^-8, 2^-7], byte 120, and 3.0 * 2^7 = 384 =
+    1.5 * 2^8 is E4M3 0 1111 100 = 0x7C, -1.0 * 2^7 = -2^7 is 1 1110 000 =
+    0xF0; the NaN stays a NaN (S.1111.111)."""
+    from fractions import Fraction
+    inf_bits = {+1: 0x7F80, -1: 0xFF80}                  # bf16 +-infinity
+    row = np.zeros(256, np.uint16)
+    row[0], row[1] = inf_bits[+1], inf_bits[-1]
+    row[2] = 0x3F80                                        # 1.0
+    row[3] = 0xC020                                        # -2.5
+    row[128] = 0x7FC0                                      # NaN
+    row[129] = 0x4040                                      # 3.0
+    row[130] = 0xBF80                                      # -1.0
+    q, s = oracle.quantize_row(row, oracle.FP8_E4M3_UE8M0)
+    assert s.tolist() == [247, 120]
+    assert q[0] == 0x7E and q[1] == 0xFE and q[2] == 0x00 and q[3] == 0x80
+    assert np.all(q[4:128] == 0x00)
+    assert (q[128] & 0x7F) == 0x7F                        # NaN, either sign
+    assert q[129] == 0x7C and q[130] == 0xF0 and np.all(q[131:] == 0x00)
+    # fp32 scales: the infinity block's scale is FLT_MAX / 448 rounded once
+    q, s = oracle.quantize_row(row, oracle.FP8_E4M3_F32_SCALE)
+    flt_max = Fraction(2**24 - 1, 2**23) * 2**127
+    exact = flt_max / 448
+    assert abs(Fraction(float(s[0])) - exact) <= exact * Fraction(1, 2**24)
+    assert q[0] == 0x7E and q[1] == 0xFE and q[2] == 0x00 and q[3] == 0x80
+    assert abs(Fraction(float(s[1])) - Fraction(3, 448)) <= Fraction(3, 448) * Fraction(1, 2**24)
+    assert (q[128] & 0x7F) == 0x7F
+    # 3.0 * (448 / 3) = 448 exactly after rounding: the block maximum maps to 448
+    assert q[129] == 0x7E

@@ -32,6 +32,7 @@ MUTANTS = {
                             "? ldexp(1.0, -10) : ldexp(1.0, ilogb(a) - 3)", 0),
     # FP8 block quantisation
     "amax_floor_dropped": ("if (amax < 1e-4f) amax = 1e-4f;", "if (amax <= 0.0f) amax = 1e-30f;", 0),
+    "amax_infinity_not_capped": ("if (amax > FLT_MAX) amax = FLT_MAX;", "", 0),
     "fp32_scale_inverted": ("float scale = amax / 448.0f;", "float scale = 448.0f / amax;", 0),
     "fp32_max_240": ("float inv = 448.0f / amax;", "float inv = 240.0f / amax;", 0),
     "ue8m0_rounds_down": ("if (bits & 0x7fffffu) biased += 1u;", "", 0),
