@@ -9,13 +9,19 @@
 // T*k ids with E buckets, done here as one kernel:
 //   1. a CTA takes a chunk of tokens (claimed through an atomic ticket, so
 //      chunks start in order and every wait below is on an earlier,
-//      already-running CTA), ranks its ids per warp with equal-key lane
-//      masks built from ballots (peers_mask) and reduces the per-warp counts
-//      in shared memory;
+//      already-running CTA; in normal mode a rank that is a single chunk
+//      waits for nobody, so its CTA index names it and its ids load at
+//      once), ranks its ids per warp with equal-key lane masks built from
+//      ballots (peers_mask) and reduces the per-warp counts in shared
+//      memory; in normal mode (R <= 64) it also forms each token's
+//      destination-rank mask, counts tokens per rank by a warp bit transpose
+//      and writes the chunk's is_token_in_rank rows as 16-byte stores;
 //   2. it publishes the chunk aggregate and looks back over the previous
-//      chunks' published (aggregate | inclusive) words, 8 at a time, to get
-//      its exclusive prefix per expert (decoupled look-back);
+//      chunks' published (aggregate | inclusive) words, kLookbackWindow at
+//      a time, to get its exclusive prefix per expert (decoupled look-back);
 //   3. it writes the per-slot results.
+// Chunks hold 2048 ids, or 8192 in normal mode once 2048-id chunks would
+// need more than one wave of a CTA per SM.
 // Normal mode scans within each source rank (get_dispatch_layout is a
 // per-rank operation).  Low-latency mode scans across all ranks in
 // (rank, token, slot) order, which directly yields the packed row
