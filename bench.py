@@ -241,13 +241,13 @@ class Runner:
                     w.R, self.cap, w.H)
         torch.cuda.synchronize()
 
-    def _layout_notify(self):
+    def _layout_notify(self, host_wait=True):
         ep, w = self.ep, self.w
         ids, E, A, nwt = self.idx, w.E, w.expert_alignment, w.num_worst_tokens
         if self.rank:   # experts' = ranks, over the per-slot destination ranks
             ep.ep_rank_ids(self.idx, w.E, self.rank_ids, self.status)
             ids, E, A, nwt = self.rank_ids, w.R, 1, -1
-        host = self.host_rows if nwt < 0 else None
+        host = self.host_rows if (nwt < 0 and host_wait) else None
         if self.fused_layout_notify:   # one launch (ep_layout_notify)
             ep.ep_layout_notify(ids, E, A, nwt, self.lay, self.nt, self.ws, host, 10000,
                                 self.status)
@@ -271,7 +271,11 @@ class Runner:
             ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
 
     def step(self, ev=None):
-        """One pass; ev = (e0, e1, e2, e3) events around dispatch / combine."""
+        """One pass; ev = (e0, e1, e2, e3) events around dispatch / combine.
+        With ev (the per-kernel split), normal mode skips the host wait for
+        the receive counts (the buffers are already sized), so the host
+        enqueues the whole step at once and no host latency falls between
+        the events."""
         ep, w, b = self.ep, self.w, self.buf
         if self.ll:
             if ev:
@@ -289,7 +293,7 @@ class Runner:
             if ev:
                 ev[3].record()
         elif self.rank:
-            self._layout_notify()
+            self._layout_notify(host_wait=ev is None)
             if ev:
                 ev[0].record()
             ep.ep_dispatch(self.x, self.rank_ids, self.lay["slot_rank"], self.nt["expert_prefix"],
@@ -306,7 +310,7 @@ class Runner:
             if ev:
                 ev[3].record()
         else:
-            self._layout_notify()
+            self._layout_notify(host_wait=ev is None)
             if ev:
                 ev[0].record()
             ep.ep_dispatch(self.x, self.idx, self.lay["slot_rank"], self.nt["expert_prefix"],
@@ -360,24 +364,29 @@ def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
     launches = ep.ep_launch_count() - launches0
     step_ms = [a.elapsed_time(b) for a, b in outer]
     # the same steps again with events between dispatch and combine (their
-    # split; the extra events cost the step a few microseconds)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    # split; the extra events cost the step a few microseconds; normal mode
+    # enqueues the step without the host wait for the receive counts)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     torch.cuda.synchronize()
     for s in range(steps):
         flush.fill_(s & 0xFF)
-        runner.step(evs[s])
+        evs[s][4].record()   # step start: layout + notify run before e[0] in normal mode
+        runner.step(evs[s][:4])
     torch.cuda.synchronize()
     disp_ms = [e[0].elapsed_time(e[1]) for e in evs]
     comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    ln_ms = [e[4].elapsed_time(e[0]) for e in evs]
     def stats_us(v):
         q = sorted(v)
         return {"median": round(statistics.median(q) * 1e3, 2), "min": round(q[0] * 1e3, 2),
-                "p90": round(q[min(len(q) - 1, int(0.9 * len(q)))] * 1e3, 2)}
+                "p90": round(q[min(len(q) - 1, int(0.9 * len(q)))] * 1e3, 2),
+                "max": round(q[-1] * 1e3, 2)}
 
     res = {"step_ms": statistics.mean(step_ms), "step_ms_min": min(step_ms),
            "step_us_stats": stats_us(step_ms), "dispatch_us_stats": stats_us(disp_ms),
            "combine_us_stats": stats_us(comb_ms),
            "dispatch_ms": statistics.mean(disp_ms), "combine_ms": statistics.mean(comb_ms),
+           "layout_notify_ms": statistics.mean(ln_ms),
            "launches": launches, "wall_s": wall}
     if e2e:
         res["e2e"] = measure_e2e(runner, steps, world, flush)
@@ -908,7 +917,7 @@ def assemble_line(args, world, head, results, clocks, peak, peak_kind):
             "dispatch_gbs": round(r["dispatch_gbs"], 1), "combine_gbs": round(r["combine_gbs"], 1),
             "dispatch_frac": round(r["dispatch_gbs"] / peak, 4),
             "combine_frac": round(r["combine_gbs"] / peak, 4),
-            "layout_notify_ms": round(r["step_ms"] - r["dispatch_ms"] - r["combine_ms"], 4),
+            "layout_notify_ms": round(r.get("layout_notify_ms", 0.0), 4),
             "gpu_launches": r["launches"],
             "roofline": roofline_of(name, wo, ro, r, peak, peak_kind, args.no_combine)}
         if r.get("launch_latency_us"):
@@ -920,8 +929,7 @@ def assemble_line(args, world, head, results, clocks, peak, peak_kind):
     line["workloads"] = others
     line["kernels_ms"] = {"dispatch": round(res["dispatch_ms"], 5),
                           "combine": round(res["combine_ms"], 5),
-                          "layout_notify": round(res["step_ms"] - res["dispatch_ms"]
-                                                 - res["combine_ms"], 5)}
+                          "layout_notify": round(res.get("layout_notify_ms", 0.0), 5)}
     if res.get("launch_latency_us"):
         line["launch_latency_us"] = res["launch_latency_us"]
     if res.get("single_call"):

@@ -9,7 +9,7 @@
 namespace ep {
 
 constexpr int kScatterMaxWarps = 16;
-constexpr int kBf16Warps = 8;      // target warps per CTA, bf16 path
+constexpr int kBf16Warps = 16;     // target warps per CTA, bf16 path (1792-channel pieces at H = 7168)
 constexpr int kFp8Warps = 16;      // target warps per CTA, FP8 path
 constexpr int kBf16Stages = 3;     // staged source pieces per warp (bf16 path)
 constexpr int kFp8InStages = 2;    // staged source pieces per warp (FP8 path)
