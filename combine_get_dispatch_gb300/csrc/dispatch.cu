@@ -632,7 +632,12 @@ static int launch_scatter_t(ScatterParams p, cudaStream_t stream, bool pdl) {
   }
   const int64_t work = std::max<int64_t>(p.n_units, p.n_pad_items);
   const int64_t want = (work + p.warps_per_cta - 1) / p.warps_per_cta;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::grid_cap(1)));
+  // one CTA per SM, on at most kScatterMaxCtas SMs unless an SM budget says
+  // otherwise: this write-heavy kernel runs 4-9 % faster on 120-132 SMs of a
+  // GB300 than on all 152, and 8-11 % slower from 134 SMs on
+  const int cap = ep_host::sm_budget_set() ? ep_host::grid_cap(1)
+                                           : std::min(ep_host::grid_cap(1), kScatterMaxCtas);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)cap));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(p.warps_per_cta * kWarp);

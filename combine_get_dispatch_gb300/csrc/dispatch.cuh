@@ -15,6 +15,7 @@ constexpr int kBf16Stages = 3;     // staged source pieces per warp (bf16 path)
 constexpr int kFp8InStages = 2;    // staged source pieces per warp (FP8 path)
 constexpr int kFp8OutStages = 2;   // staged E4M3 pieces per warp
 constexpr size_t kScatterSmemBudget = 200 * 1024;
+constexpr int kScatterMaxCtas = 128;   // default grid cap of the scatter (measured sweep)
 constexpr int kPadChunkRows = 1024;
 constexpr int kScaleColThreads = 256;
 
