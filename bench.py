@@ -44,12 +44,19 @@ HEADLINE = "large"
 DERIVED = {"prefill_v1": ("prefill", {"mode": "rank"})}
 
 
-def workload(name: str):
+def workload(name: str, tokens_per_rank: int = 0):
+    """A workload by name; tokens_per_rank > 0 scales its T_r (profiling only)."""
     from combine_get_dispatch_gb300 import synth
     if name in DERIVED:
         base, changes = DERIVED[name]
-        return synth.scaled(synth.WORKLOADS[base], name=name, **changes)
-    return synth.WORKLOADS[name]
+        w = synth.scaled(synth.WORKLOADS[base], name=name, **changes)
+    else:
+        w = synth.WORKLOADS[name]
+    if tokens_per_rank > 0:
+        w = synth.scaled(w, T_r=tokens_per_rank,
+                         max_tokens_per_rank=max(w.max_tokens_per_rank, tokens_per_rank),
+                         num_worst_tokens=(w.R * tokens_per_rank if w.num_worst_tokens >= 0 else -1))
+    return w
 FLUSH_BYTES = 512 << 20
 
 
@@ -767,7 +774,7 @@ def run_sm_sweep(args, local_rank):
     budgets = [int(b) for b in args.sm_sweep.split(",") if b.strip()]
     try:
         for name in [n.strip() for n in args.workloads.split(",") if n.strip()]:
-            w = workload(name)
+            w = workload(name, args.tokens_per_rank)
             runner = Runner(w, dev)
             row_in = 2 * w.H
             row_out = (2 * w.H if w.fp8_mode == 0
@@ -809,12 +816,7 @@ def run_ours(args, rank, world, local_rank):
     results = {}
     clocks = None
     for name in names:
-        w = workload(name)
-        if args.tokens_per_rank > 0:
-            w = synth.scaled(w, T_r=args.tokens_per_rank,
-                             max_tokens_per_rank=max(w.max_tokens_per_rank, args.tokens_per_rank),
-                             num_worst_tokens=(w.R * args.tokens_per_rank
-                                               if w.num_worst_tokens >= 0 else -1))
+        w = workload(name, args.tokens_per_rank)
         runner = Runner(w, dev, with_combine=not args.no_combine,
                         fused_layout_notify=not args.separate_layout_notify)
         sampler = ClockSampler(local_rank) if name == head else None
