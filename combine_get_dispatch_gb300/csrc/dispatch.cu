@@ -50,9 +50,13 @@ namespace ep {
 
 // ------------------------------------------------------------------ warp pipeline
 
-// One warp's TMA pipeline over its units u = first + i * stride (i < count);
-// unit u is piece u % P of token u / P.  Units are walked with incremental
-// (token, piece) cursors, so the loop does no integer division.
+// One warp's TMA pipeline over a sequence of units; unit u is piece u % P of
+// token u / P.  The sequence (UnitSeq below) starts with kSeqStatic units
+// first + j * stride, and continues either the same way or, with a
+// workspace counter, with units claimed one at a time as the warp goes: SMs
+// of a GB300 do not all stream at the same rate (a static split of the
+// 152 SMs' work measured CTAs finishing between 0.62x and 1.0x of the
+// slowest one's time), so a warp on a faster SM takes more units.
 struct Pipe {
   uint8_t* s_in;            // [NS][in_bytes] staged bf16 source pieces
   uint8_t* s_out;           // [NO][out_bytes] staged E4M3 pieces
@@ -64,8 +68,8 @@ struct Pipe {
   uint8_t* scale_rows;
   int scale_row_bytes;
   int32_t* status;
-  int32_t first, stride, count;
-  int32_t stride_g, stride_pc;   // stride / P, stride % P
+  int32_t first, stride, n_units;
+  uint32_t* claim;   // workspace counter of dynamically claimed units, or null (static sequence)
 };
 
 struct Cursor {
@@ -79,14 +83,89 @@ __device__ __forceinline__ Cursor cursor_at(const Pipe& q, int32_t u) {
   return c;
 }
 
-__device__ __forceinline__ void cursor_next(const Pipe& q, Cursor& c) {
-  c.g += q.stride_g;
-  c.pc += q.stride_pc;
-  if (c.pc >= q.P) {
-    c.pc -= q.P;
-    c.g += 1;
+constexpr int kSeqStatic = 4;    // units per warp assigned by index before any claim
+constexpr int kClaimMax = 8;     // units per claim at most
+
+// A warp's units at positions i, i + 1, i + 2 (warp-uniform; -1 = the
+// sequence has ended) and where the later ones come from: the static units
+// first + j * stride for j < kSeqStatic, then batches claimed from the
+// workspace counter (unit = kSeqStatic * stride + counter value).  Claims
+// are guided: a batch holds max(1, min(kClaimMax, remaining / (4 * stride)))
+// units, so early claims are few and large and the last ones single units
+// (the counter is not contended and the warps end together).  The next
+// batch's claim goes out as soon as the current batch is taken, a whole
+// batch ahead of its use.  Once a position is past the end every later one
+// is too.
+struct UnitSeq {
+  int32_t u0, u1, u2;
+  int32_t next;       // position of the next unit to bring in
+  int32_t nb, ne;     // dynamic units [nb, ne) taken but not yet handed out
+  uint32_t pend;      // lane 0: counter value returned by the claim in flight
+  int32_t pend_n;     // size of that claim (0: none in flight)
+  bool ended;
+
+  __device__ __forceinline__ int32_t static_unit(const Pipe& q, int32_t j) const {
+    const int64_t u = (int64_t)q.first + (int64_t)j * q.stride;
+    return u < q.n_units ? (int32_t)u : -1;
   }
-}
+  __device__ __forceinline__ int64_t dyn_base(const Pipe& q) const {
+    return (int64_t)kSeqStatic * q.stride;
+  }
+  // Issue a claim sized for `remaining` units left after the counter value seen.
+  __device__ __forceinline__ void claim(const Pipe& q, int64_t remaining, int lane) {
+    int64_t b = remaining / (4 * (int64_t)q.stride);
+    b = b < 1 ? 1 : (b > kClaimMax ? kClaimMax : b);
+    pend_n = (int32_t)b;
+    if (lane == 0) pend = atomicAdd(q.claim, (uint32_t)b);
+  }
+  __device__ __forceinline__ int32_t take(const Pipe& q, int lane) {
+    if (ended) return -1;
+    if (next < kSeqStatic || q.claim == nullptr) {
+      const int32_t u = static_unit(q, next++);
+      if (u < 0) ended = true;
+      return u;
+    }
+    ++next;
+    if (nb >= ne) {   // the claimed batch: wait for it, and claim the following one
+      const uint32_t c = __shfl_sync(0xffffffffu, pend, 0);
+      const int64_t lo = dyn_base(q) + c;
+      const int64_t hi = lo + pend_n;
+      pend_n = 0;
+      if (lo >= q.n_units) {
+        ended = true;
+        return -1;
+      }
+      nb = (int32_t)lo;
+      ne = (int32_t)(hi < q.n_units ? hi : q.n_units);
+      claim(q, q.n_units - hi, lane);
+    }
+    return nb++;
+  }
+  __device__ __forceinline__ void init(const Pipe& q, int lane) {
+    next = 0;
+    nb = ne = 0;
+    pend = 0u;
+    pend_n = 0;
+    ended = false;
+    u0 = take(q, lane);
+    u1 = take(q, lane);
+    u2 = take(q, lane);
+    // the first batch is claimed now, kSeqStatic positions ahead of its use
+    // (only if the static units are not already past the end)
+    if (q.claim != nullptr && !ended) claim(q, q.n_units - dyn_base(q), lane);
+  }
+  // Lane 0 waits for a claim still in flight (the counter must have taken
+  // every claim before the launch's last CTA resets it).
+  __device__ __forceinline__ void settle(int lane) const {
+    if (lane == 0 && pend_n > 0) asm volatile("" ::"r"(pend) : "memory");
+  }
+  // Move to the next position.
+  __device__ __forceinline__ void shift(const Pipe& q, int lane) {
+    u0 = u1;
+    u1 = u2;
+    u2 = take(q, lane);
+  }
+};
 
 template <int kMode>
 struct PipeDepth {
@@ -107,23 +186,19 @@ __device__ __forceinline__ void pipe_issue_load(const Pipe& q, int32_t i, const 
               q.x + (int64_t)c.g * q.H * 2 + (int64_t)c.pc * q.Hp * 2, bytes, b);
 }
 
-// Barrier set-up and the first source loads (they depend on nothing but x).
-// Returns the cursor of the next unit to load.
+// Barrier set-up and the source loads of positions 0 and 1 (static units:
+// they depend on nothing but x).
 template <int kMode>
-__device__ __forceinline__ Cursor pipe_prologue(const Pipe& q, int lane) {
-  Cursor c = cursor_at(q, q.first);
-  if (q.count <= 0) return c;
-  const int32_t pro = min((int32_t)PipeDepth<kMode>::kPrologue, q.count);
+__device__ __forceinline__ void pipe_prologue(const Pipe& q, const UnitSeq& seq, int lane) {
+  static_assert(PipeDepth<kMode>::kPrologue == 2, "loads run two positions ahead (UnitSeq holds three)");
+  if (seq.u0 < 0) return;
   if (lane == 0) {
     for (int s = 0; s < PipeDepth<kMode>::NS; ++s) mbar_init(&q.bar[s], 1);
     fence_barrier_init();
-  }
-  for (int32_t i = 0; i < pro; ++i) {
-    if (lane == 0) pipe_issue_load<kMode>(q, i, c);
-    cursor_next(q, c);
+    pipe_issue_load<kMode>(q, 0, cursor_at(q, seq.u0));
+    if (seq.u1 >= 0) pipe_issue_load<kMode>(q, 1, cursor_at(q, seq.u1));
   }
   __syncwarp();
-  return c;
 }
 
 // Run the pipeline.  D supplies each unit's destinations in two stages so
@@ -131,31 +206,26 @@ __device__ __forceinline__ Cursor pipe_prologue(const Pipe& q, int lane) {
 //   d.pre(g, lane)              first-level value for slot lane (lane < k)
 //   d.fin(g, pc, lane, pre)     flat receive row of slot lane, or -1
 template <int kMode, class D>
-__device__ __forceinline__ void pipe_run(const Pipe& q, const D& d, int lane, Cursor ld) {
+__device__ __forceinline__ void pipe_run(const Pipe& q, const D& d, int lane, UnitSeq& seq) {
   constexpr bool kFp8 = PipeDepth<kMode>::kFp8;
   constexpr int NS = PipeDepth<kMode>::NS;
   constexpr int NO = PipeDepth<kMode>::NO;
   constexpr int kEs = kMode == EP_FP8_E4M3_F32_SCALE ? 4 : 1;
-  const int32_t n = q.count;
-  if (n <= 0) return;
+  if (seq.u0 < 0) return;
   const int64_t row_bytes = kFp8 ? (int64_t)q.H : (int64_t)q.H * 2;
-  Cursor cur = cursor_at(q, q.first);
-  Cursor c1 = cur, c2 = cur;
-  cursor_next(q, c1);
-  cursor_next(q, c2);
-  cursor_next(q, c2);
-  int64_t pre_a = d.pre(cur.g, lane);
-  int64_t pre_b = n > 1 ? d.pre(c1.g, lane) : -1;
-  int32_t ld_i = min((int32_t)PipeDepth<kMode>::kPrologue, n);   // next unit to load
+  int64_t pre_a = d.pre(seq.u0 / q.P, lane);
+  int64_t pre_b = seq.u1 >= 0 ? d.pre(seq.u1 / q.P, lane) : -1;
+  int32_t ld_i = seq.u1 >= 0 ? 2 : 1;   // positions whose loads are out (the prologue's)
 
   bool failed = false;
   int32_t i = 0;
-  for (; i < n; ++i) {
+  for (; seq.u0 >= 0; ++i) {
+    const Cursor cur = cursor_at(q, seq.u0);
     const int hc = min(q.Hp, q.H - cur.pc * q.Hp);
     const int s = i % NS;
     const int32_t my_f = d.fin(cur.g, cur.pc, lane, pre_a);
     pre_a = pre_b;
-    if (i + 2 < n) pre_b = d.pre(c2.g, lane);
+    if (seq.u2 >= 0) pre_b = d.pre(seq.u2 / q.P, lane);
     const bool landed = mbar_wait_bounded(&q.bar[s], (uint32_t)((i / NS) & 1));
     if (!__all_sync(0xffffffffu, landed)) {   // warp-uniform decision
       set_status(q.status, EP_ERR_TIMEOUT);
@@ -169,15 +239,11 @@ __device__ __forceinline__ void pipe_run(const Pipe& q, const D& d, int lane, Cu
         const int32_t f = __shfl_sync(0xffffffffu, my_f, j);
         if (lane == 0 && f >= 0) tma_store_1d(q.recv_x + f * row_bytes + col, src, (uint32_t)hc * 2u);
       }
-      // unit i-1's stores have read their stage: refill it with unit i+NS-1
+      // position i-1's stores have read their stage: refill it with position i+2
       if (lane == 0) {
         tma_commit();
         tma_wait_read<1>();
-        if (ld_i < n) pipe_issue_load<kMode>(q, ld_i, ld);
-      }
-      if (ld_i < n) {
-        ++ld_i;
-        cursor_next(q, ld);
+        if (seq.u2 >= 0) pipe_issue_load<kMode>(q, i + 2, cursor_at(q, seq.u2));
       }
       __syncwarp();
     } else {
@@ -208,34 +274,30 @@ __device__ __forceinline__ void pipe_run(const Pipe& q, const D& d, int lane, Cu
       }
       fence_proxy_async_smem();
       __syncwarp();
-      // source stage s was fully read: refill it with unit i+NS
-      if (lane == 0 && ld_i < n) pipe_issue_load<kMode>(q, ld_i, ld);
-      if (ld_i < n) {
-        ++ld_i;
-        cursor_next(q, ld);
-      }
+      // source stage s was fully read: refill it with position i+2
+      if (lane == 0 && seq.u2 >= 0) pipe_issue_load<kMode>(q, i + 2, cursor_at(q, seq.u2));
       for (int j = 0; j < q.k; ++j) {
         const int32_t f = __shfl_sync(0xffffffffu, my_f, j);
         if (lane == 0 && f >= 0) tma_store_1d(q.recv_x + f * row_bytes + col, dst, (uint32_t)hc);
       }
       if (lane == 0) tma_commit();
     }
-    cur = c1;
-    c1 = c2;
-    cursor_next(q, c2);
+    if (seq.u2 >= 0) ld_i = i + 3;
+    seq.shift(q, lane);
   }
   if (failed && lane == 0) {
     // drain (bounded) the loads this warp still has in flight
     for (int32_t r = i; r < ld_i; ++r) mbar_wait_bounded(&q.bar[r % NS], (uint32_t)((r / NS) & 1));
   }
+  seq.settle(lane);
   if (lane == 0) tma_wait_all();
 }
 
-// Carve this warp's pipeline out of the CTA's shared memory; units
-// first, first + stride, ... (count of them).
+// Carve this warp's pipeline out of the CTA's shared memory; its units
+// start with first, first + stride, ... (UnitSeq).
 template <int kMode>
 __device__ __forceinline__ Pipe make_pipe(uint8_t* smem, const ScatterParams& p, int warp,
-                                          int32_t first, int32_t stride, int32_t count) {
+                                          int32_t first, int32_t stride) {
   Pipe q;
   uint8_t* ws = smem + (size_t)warp * p.warp_smem;
   q.s_in = ws;
@@ -254,9 +316,8 @@ __device__ __forceinline__ Pipe make_pipe(uint8_t* smem, const ScatterParams& p,
   q.status = p.status;
   q.first = first;
   q.stride = stride;
-  q.count = count;
-  q.stride_g = stride / p.P;
-  q.stride_pc = stride - q.stride_g * p.P;
+  q.n_units = (int32_t)p.n_units;
+  q.claim = p.claim;
   return q;
 }
 
@@ -344,21 +405,34 @@ __global__ void __launch_bounds__(kScatterMaxWarps * kWarp) k_scatter(ScatterPar
   if (kMode != EP_FP8_NONE) pdl_launch_dependents();   // the scale-column pass may launch
   const int32_t gw = blockIdx.x * p.warps_per_cta + warp;
   const int32_t W = gridDim.x * p.warps_per_cta;
-  const int32_t n_units = (int32_t)p.n_units;
-  const int32_t count = gw < n_units ? (n_units - gw + W - 1) / W : 0;
-  Pipe q = make_pipe<kMode>(smem, p, warp, gw, W, count);
-  const Cursor ld = pipe_prologue<kMode>(q, lane);
-  if (kLL) {
-    pdl_wait();   // combine_idx of the layout kernel is read from here on
-    pipe_run<kMode>(q, PackedDest{&p}, lane, ld);
-    return;
-  }
-  // launched as a programmatic dependent of the layout + notify kernel, the
-  // first x pieces went out above; the prefix tables are read from here on
-  // (a no-op after an ordinary launch)
+  Pipe q = make_pipe<kMode>(smem, p, warp, gw, W);
+  UnitSeq seq;
+  seq.init(q, lane);
+  pipe_prologue<kMode>(q, seq, lane);
+  // low latency: combine_idx of the layout kernel is read from here on;
+  // normal mode launched as a programmatic dependent of the layout + notify
+  // kernel: the first x pieces went out above, the prefix tables are read
+  // from here on (a no-op after an ordinary launch)
   pdl_wait();
-  pipe_run<kMode>(q, NormalDest{&p}, lane, ld);
-  pad_fill(p, gw, W, lane);
+  if (kLL) {
+    pipe_run<kMode>(q, PackedDest{&p}, lane, seq);
+  } else {
+    pipe_run<kMode>(q, NormalDest{&p}, lane, seq);
+    pad_fill(p, gw, W, lane);
+  }
+  if (p.claim != nullptr) {   // the last CTA out resets the claim counter for the next launch
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();   // every claim of this CTA is performed before its arrival
+      const uint32_t d = atomicAdd(&p.claim[1], 1u);
+      if (d >= gridDim.x) set_status(p.status, EP_ERR_STATE);   // workspace not cleaned
+      if (d == gridDim.x - 1) {
+        __threadfence();
+        p.claim[0] = 0u;
+        p.claim[1] = 0u;
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ scale columns
@@ -632,12 +706,7 @@ static int launch_scatter_t(ScatterParams p, cudaStream_t stream, bool pdl) {
   }
   const int64_t work = std::max<int64_t>(p.n_units, p.n_pad_items);
   const int64_t want = (work + p.warps_per_cta - 1) / p.warps_per_cta;
-  // one CTA per SM, on at most kScatterMaxCtas SMs unless an SM budget says
-  // otherwise: this write-heavy kernel runs 4-9 % faster on 120-132 SMs of a
-  // GB300 than on all 152, and 8-11 % slower from 134 SMs on
-  const int cap = ep_host::sm_budget_set() ? ep_host::grid_cap(1)
-                                           : std::min(ep_host::grid_cap(1), kScatterMaxCtas);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)cap));
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)ep_host::grid_cap(1)));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(p.warps_per_cta * kWarp);
@@ -743,6 +812,7 @@ static int dispatch_normal(const void* x, const int64_t* topk_idx, const int32_t
     p.scale_row_bytes = ep::scale_row_bytes(H, es);
   }
   p.status = status;
+  p.claim = workspace != nullptr ? static_cast<uint32_t*>(workspace) + ep::kCtlClaim : nullptr;
   p.tail_chunks = (int)((cap_rows + ep::kPadChunkRows - 1) / ep::kPadChunkRows);
   p.n_pad_items = (int64_t)R * p.E_l + (int64_t)R * p.tail_chunks;
   rc = ep::launch_scatter(p, fp8_mode, false, s, pdl);

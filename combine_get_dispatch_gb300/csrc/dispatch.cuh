@@ -15,7 +15,10 @@ constexpr int kBf16Stages = 3;     // staged source pieces per warp (bf16 path)
 constexpr int kFp8InStages = 2;    // staged source pieces per warp (FP8 path)
 constexpr int kFp8OutStages = 2;   // staged E4M3 pieces per warp
 constexpr size_t kScatterSmemBudget = 200 * 1024;
-constexpr int kScatterMaxCtas = 128;   // default grid cap of the scatter (measured sweep)
+// Workspace control words (uint32 at the start of the workspace): 0-3 the
+// layout kernel's ticket / done / epoch / abort, 8-9 the single-launch
+// low-latency kernel's grid barrier, 10-11 the scatter's unit claims.
+constexpr int kCtlClaim = 10;
 constexpr int kPadChunkRows = 1024;
 constexpr int kScaleColThreads = 256;
 
@@ -44,6 +47,7 @@ struct ScatterParams {
   int64_t n_units;         // T * P
   int64_t n_pad_items;
   int tail_chunks;
+  uint32_t* claim;         // [2] workspace words: unit claim counter, CTAs done; null: static split
 };
 
 __host__ __device__ inline uint32_t round128(uint32_t v) { return (v + 127u) / 128u * 128u; }

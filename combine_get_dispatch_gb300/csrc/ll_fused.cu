@@ -61,7 +61,7 @@ constexpr int kFusedBarBytes = 2 * kFusedWarps * kFusedMaxPerWarp * 8;   // load
 constexpr size_t kFusedSmemCap = 225 * 1024;
 static_assert(kRankWarps == kFusedWarps - kQuantWarps, "FP8: the rank warps are the store warps");
 static_assert(kFusedMaxPerWarp <= kWarp, "a warp issues its pieces one per lane");
-constexpr int kCtlArrive = 8;            // workspace control words of this kernel
+constexpr int kCtlArrive = 8;            // workspace control words of this kernel (see kCtlClaim)
 constexpr int kCtlExit = 9;
 
 // Wait (bounded, kWaitNs) until a grid counter reaches n; false on timeout.
@@ -727,6 +727,7 @@ extern "C" int ep_ll_dispatch(const void* x, const int64_t* topk_idx, int R, int
     p.scale_row_bytes = ep::scale_row_bytes(H, es);
   }
   p.status = status;
+  p.claim = static_cast<uint32_t*>(workspace) + ep::kCtlClaim;
   p.n_pad_items = 0;
   if (p.T == 0) return EP_OK;
   rc = ep::launch_scatter(p, fp8_mode, true, s);
