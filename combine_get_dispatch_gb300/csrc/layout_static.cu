@@ -1,10 +1,9 @@
 // layout_static.cu -- ep_get_dispatch_layout_no_alloc: get_dispatch_layout
 // for callers that cannot allocate device memory.
 //
-// Some callers may not call cudaMalloc (or any allocator) at all: code that
-// runs while a CUDA graph is being captured, code inside a custom memory
-// pool or allocator callback, and runtimes that hand the library fixed
-// buffers and forbid it from touching the device heap.  They still need the
+// Some callers may not call cudaMalloc (or any allocator) at all: code inside
+// a custom memory pool or allocator callback, and runtimes that hand the
+// library fixed buffers and forbid it from touching the device heap.  They still need the
 // layout kernel, whose decoupled look-back keeps per-chunk words and ticket
 // counters in scratch memory.  This entry point keeps that scratch in a
 // file-scope __device__ array of kStaticScratchBytes, so the caller passes
@@ -18,9 +17,8 @@
 //  - the array keeps the last call's contents, so each call first clears the
 //    part it uses (a stream-ordered memset, no allocation);
 //  - the first call on a device looks the array's device address up with
-//    cudaGetSymbolAddress (with that device current); make that first call
-//    before any stream capture begins.  The address is kept for the life of
-//    the process, so the library must not be used on a device after
+//    cudaGetSymbolAddress (with that device current).  The address is kept
+//    for the life of the process, so the library must not be used on a device after
 //    cudaDeviceReset on it;
 //  - the stream must belong to the current device (the array looked up is
 //    the current device's); a stream of another device is refused with

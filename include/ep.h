@@ -81,8 +81,9 @@ extern "C" {
  * ep_ll_dispatch need for problems up to (R, T_r, k, E, H); 0 for invalid
  * sizes.  The workspace holds the cross-block prefix (decoupled look-back)
  * state of the layout kernels, the per-token FP8 scales staged between the
- * scatter and the column-major scale pass, and the grid-barrier words of the
- * single-launch low-latency path.  It must be zeroed once with
+ * scatter and the column-major scale pass, the grid-barrier words of the
+ * single-launch low-latency path and the work counter that spreads the
+ * scatter's (token, piece) units over the SMs as they finish.  It must be zeroed once with
  * ep_clean_ll_buffer before its first use, after which every call leaves it
  * ready for the next.  Calls that share one workspace must be ordered on
  * one stream (overlapping calls race).  16-byte aligned. */
@@ -104,8 +105,7 @@ int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E
                            void* stream);
 
 /* ep_get_dispatch_layout for callers that cannot allocate device memory
- * (graph capture in progress, allocator callbacks, runtimes that forbid the
- * library any allocation).  No counterpart in the article: it is the same
+ * (allocator callbacks, runtimes that forbid the library any allocation).  No counterpart in the article: it is the same
  * layout computation, same arguments and outputs as ep_get_dispatch_layout
  * minus the workspace, which is replaced by a 4 MiB array inside libep
  * (held on every GPU that loads the library, until the process exits).
@@ -117,8 +117,7 @@ int ep_get_dispatch_layout(const int64_t* topk_idx, int R, int T_r, int k, int E
  *    (stream-ordered); calls that overlap on the GPU race, so order them on
  *    one stream.
  *  - The first call on a device looks up the array's address with that
- *    device current; make it before any stream capture begins.  The address
- *    is kept until the process exits: do not use the library on a device
+ *    device current.  The address is kept until the process exits: do not use the library on a device
  *    after cudaDeviceReset on it.
  *  - `stream` must belong to the current device (NULL: the current
  *    device's default stream); a stream of another device returns
@@ -191,7 +190,9 @@ int ep_layout_notify_dispatch(const void* x, const int64_t* topk_idx, int R, int
  *                alignment padding and past the last row
  *   combine_idx  [R, T_r, k] int32: r*cap_rows + row, -1 for an unused slot
  *   workspace    ep_workspace_size bytes (required when fp8_mode > 0, may be
- *                NULL for bf16)
+ *                NULL for bf16: the scatter then splits its units statically
+ *                over the CTAs, which is slower when SMs run at different
+ *                speeds)
  * A row at or past cap_rows is not written (EP_ERR_CAPACITY, slot -1).
  * Rows of recv_x that no slot fills are left untouched; scale entries of
  * rows that hold no token are unspecified. */

@@ -1,6 +1,6 @@
 """ep_get_dispatch_layout_no_alloc: the layout for callers that may not
-allocate device memory (graph capture, allocator callbacks, runtimes that
-forbid the library any allocation).  Called through the C ABI and compared
+allocate device memory (allocator callbacks, runtimes that forbid the
+library any allocation).  Called through the C ABI and compared
 with the oracle and with ep_get_dispatch_layout (caller-provided workspace)
 on calls in a row -- each call reuses the static scratch the one before
 left behind.
