@@ -235,6 +235,29 @@ def test_handle_reuse_across_dispatches(fp8_mode):
 
 
 @pytest.mark.parametrize("fp8_mode", [1, 2])
+def test_workspace_reused_across_batch_sizes(fp8_mode):
+    """One workspace, sized for the largest batch, serves FP8 dispatches of
+    several batch sizes in turn (as a serving loop with a varying batch
+    does).  The staged scales and the layout's look-back words sit at
+    offsets that move with the batch size, so each call finds bytes another
+    size left behind; every call must still give the oracle's rows and
+    column-major scales."""
+    base = synth.scaled(synth.WORKLOADS["skewed"], T_r=64, fp8_mode=fp8_mode)
+    ws = ep.alloc_workspace(base.R, 64, base.k, base.E, base.H)
+    for i, T_r in enumerate((64, 24, 64, 8, 40, 64)):
+        w = synth.scaled(synth.WORKLOADS["skewed"], T_r=T_r, fp8_mode=fp8_mode)
+        x_dev, x_host, idx_dev, idx, _, _ = inputs(w, seed=10 + i)
+        lay = gpu_layout(idx_dev, w.E)
+        nt = gpu_notify(lay, w.E, 1, -1)
+        torch.cuda.synchronize()
+        cap = max(1, int(np_(nt["psum"])[:, -1].max()))
+        d = gpu_dispatch(x_dev, idx_dev, lay, nt, w.E, fp8_mode, cap, ws=ws)
+        torch.cuda.synchronize()
+        assert ep.ep_read_status(d["status"]) == ep.EP_OK, T_r
+        _compare_full(w, x_host, idx, d, cap, 1)
+
+
+@pytest.mark.parametrize("fp8_mode", [1, 2])
 @pytest.mark.parametrize("pad,A", [(16, 1), (16, 4), (2, 1), (1, 1), (0, 128)])
 def test_scale_columns_quad_and_single_row_paths(pad, A, fp8_mode):
     """With ue8m0 scales the column pass writes 4 rows per thread (one 4-byte
