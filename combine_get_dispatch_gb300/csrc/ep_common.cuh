@@ -50,6 +50,23 @@ __device__ __forceinline__ int32_t ld_cg_i32(const int32_t* p) {
   return v;
 }
 
+// atomicAdd with acquire-release semantics at GPU scope: one instruction
+// where a fence, a relaxed atomic and a second fence would otherwise be
+// three memory round trips (the arrival of a last-one-out pattern).
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// atomicAdd with release semantics at GPU scope (the arrival at a barrier
+// whose waiters then read with acquire loads).
+__device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

@@ -399,8 +399,10 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
   __shared__ int s_last;
   __syncthreads();
   if (tid == 0) {
-    if (p.fuse_notify) __threadfence();   // this CTA's count rows, before the arrival
-    const uint32_t d = atomicAdd(&p.ctl[1], 1u);
+    // fused notify: the arrival releases this CTA's count rows (its threads
+    // wrote them before the barrier above) and, for the last CTA, acquires
+    // everyone else's before the reads below
+    const uint32_t d = p.fuse_notify ? atom_add_acq_rel_u32(&p.ctl[1], 1u) : atomicAdd(&p.ctl[1], 1u);
     if (d >= (uint32_t)p.num_chunks) set_status(p.status, EP_ERR_STATE);   // not cleaned
     const bool last = d == (uint32_t)p.num_chunks - 1;
     if (last) {
@@ -408,7 +410,6 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) k_layout(LayoutParams p) {
       p.ctl[1] = 0;
       p.ctl[2] = ld_relaxed_u32(&p.ctl[2]) + 1;   // the next launch's epoch
       p.ctl[3] = 0;
-      if (p.fuse_notify) __threadfence();   // ... and everyone else's, before the reads
     }
     s_last = last;
   }
