@@ -664,11 +664,14 @@ int launch_scale_columns(const ScaleColParams& p, bool ll, int fp8_mode, cudaStr
 // ------------------------------------------------------------------ launch
 
 // Small FP8 batches: pieces shrink (to kMinFp8Piece channels at the least)
-// until every warp of the launch has about kMinUnitsPerWarp units.  In a
-// short kernel a warp's first loads and last stores are a large share of its
-// time; the skewed workload (8192 tokens, H = 4096) gets 6.7 units per warp
-// with the 2048-channel pieces that fit, 13.5 with 1024-channel ones, and its
-// dispatch runs 4.5 % faster (768-channel pieces were slower again).
+// until every warp of the launch has about kMinUnitsPerWarp units.  The
+// skewed workload (8192 tokens, H = 4096) gets 6.7 units per warp with the
+// 2048-channel pieces that fit, 13.5 with 1024-channel ones; measured in the
+// timed step (L2 dirty after the flush), the scatter alone takes 52.2 us
+// instead of 53.3 and the column pass behind it 6.7 instead of 8.1, the
+// dispatch 58.9 instead of 61.4 (768-channel pieces were slower again).
+// Cold and serialised under ncu the scatter alone is the slower one (55 us
+// against 49): the gain is in the conditions of the step.
 constexpr int kMinFp8Piece = 1024;
 constexpr int kMinUnitsPerWarp = 16;
 
