@@ -11,7 +11,9 @@
 //
 // Launched with programmatic dependent launch: it waits (griddepcontrol)
 // for the kernel before it -- the dispatch that wrote combine_idx -- to
-// complete, but its CTAs can be resident by then, which hides the launch.
+// complete.  The library's kernels before it do not trigger it early: its
+// CTAs would then be placed on whichever SMs free up first, several to an
+// SM, and the static split of the items over them would run unevenly.
 //
 // One warp handles one (token, 512-channel segment) item: every lane issues
 // all k row loads of its 2 x 16 bytes before the first fma (k*2 independent

@@ -517,8 +517,10 @@ __global__ void __launch_bounds__(kFusedWarps * kWarp, 1) k_ll_fused(FusedParams
     sync();   // s_passed is read by the whole group
     if (s_passed) fused_expert_outputs<kFp8, kEs>(p, cta, grid, tid, kGroup, s_P, s_lo, sync);
   }
-  __syncthreads();
-  pdl_launch_dependents();   // a dependent combine may take its place as this drains
+  // No early trigger of the dependent combine: its CTAs would be placed on
+  // the SMs this kernel frees first, several to an SM, and its static split
+  // of the tokens over them then runs unevenly (measured: decode step 89.4-
+  // 90.3 us with the trigger here, 76.3-76.6 without).
   if (tid == 0) {   // the last CTA out resets the barrier
     const uint32_t d = atomicAdd(&p.ctl[kCtlExit], 1u);
     if (d == (uint32_t)grid - 1) {
