@@ -714,12 +714,14 @@ static void plan_pipeline(ScatterParams& p, int fp8_mode, int target_warps, size
   p.warps_per_cta = (int)std::max<size_t>(1, std::min<size_t>((size_t)kScatterMaxWarps, budget / wb));
 }
 
-// The scatter is persistent: one CTA per SM.  Its shared-memory request is at
-// least kScatterMinSmem, over half of an SM's, so that no SM ever holds two
-// of its CTAs -- which a programmatic dependent launch behind the layout
-// kernel would otherwise do while the layout's CTAs still hold other SMs
-// (a small FP8 batch needs only ~100 KB; measured with two CTAs to an SM:
-// the skewed single-call step 157-158 us instead of ~153).
+// The scatter is persistent: one CTA per SM.  Launched as a programmatic
+// dependent of the layout kernel, its shared-memory request is at least
+// kScatterMinSmem, over half of an SM's, so that no SM holds two of its CTAs
+// -- which the early launch would otherwise do while the layout's CTAs still
+// hold other SMs (a small FP8 batch needs only ~100 KB; measured with two
+// CTAs to an SM: the skewed single-call step 158.7 us instead of 152.6).  An
+// ordinary launch starts on free SMs and is not padded (padded, the skewed
+// dispatch took 60.1 us instead of 58.3).
 constexpr size_t kScatterMinSmem = 120 * 1024;
 static_assert(kScatterMinSmem <= kScatterSmemBudget, "the pad stays within the planned budget");
 
@@ -728,7 +730,7 @@ static int launch_scatter_t(ScatterParams p, cudaStream_t stream, bool pdl) {
   plan_pipeline(p, kMode, kMode == EP_FP8_NONE ? kBf16Warps : kFp8Warps, kScatterSmemBudget);
   p.n_units = p.T * p.P;
   if (p.n_units > INT32_MAX) return EP_ERR_INVALID_ARG;
-  const size_t smem = std::max((size_t)p.warps_per_cta * p.warp_smem, kScatterMinSmem);
+  const size_t smem = std::max((size_t)p.warps_per_cta * p.warp_smem, pdl ? kScatterMinSmem : (size_t)0);
   {
     const int rc = ep_host::ensure_max_smem(reinterpret_cast<const void*>(k_scatter<kMode, kLL>), (int)kScatterSmemBudget + 1024);
     if (rc != EP_OK) return rc;
