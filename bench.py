@@ -649,6 +649,14 @@ def oracle_step(w, x_bits, idx, wts, y_rows, tokens_per_rank: int):
     ws = np.ascontiguousarray(wts[:, :tokens_per_rank])
     if w.mode == "ll":
         d = oracle.ll_dispatch(xs, ids, w.E, w.max_tokens_per_rank, w.fp8_mode, fill=None)
+    elif w.mode == "rank":   # once-per-rank layout: at most one row per (token, rank)
+        d = oracle.rank_dispatch(xs, ids, ws, w.E, w.fp8_mode, w.R * tokens_per_rank, fill=None)
+        cidx = d["combine_idx"]
+        m = cidx >= 0
+        remap = np.full(cidx.shape, -1, np.int32)
+        remap[m] = np.arange(int(m.sum()), dtype=np.int32)
+        oracle.rank_combine(y_rows[: int(m.sum())], remap, w.H)
+        return w.R * tokens_per_rank
     else:
         lay = oracle.layout(ids, w.R, w.E)
         nt = oracle.notify(lay["num_tokens_per_rank"], lay["num_tokens_per_expert"], w.R, w.E,
@@ -693,7 +701,7 @@ def oracle_sample_tokens(w) -> int:
     return max(1, min(w.T_r, 512 // w.R))
 
 
-def cpu_baseline(w, budget_s: float = 12.0):
+def cpu_baseline(w, budget_s: float = 12.0, alg_bytes_per_token: float = 0.0):
     import numpy as np
 
     import oracle
@@ -712,10 +720,13 @@ def cpu_baseline(w, budget_s: float = 12.0):
             if time.perf_counter() - t0 >= budget_s or reps >= 500:
                 break
         el = time.perf_counter() - t0
-    return {"value": done / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": (f"{reps} x oracle dispatch+combine of the first {tpr} tokens of each of "
-                       f"the {w.R} ranks ({w.R * tpr} tokens, 1/{w.T_r // tpr} of the workload), "
-                       f"single-threaded C pinned to one core, {el:.1f} s")}
+    out = {"value": done / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": (f"{reps} x oracle dispatch+combine of the first {tpr} tokens of each of "
+                      f"the {w.R} ranks ({w.R * tpr} tokens, 1/{w.T_r // tpr} of the workload), "
+                      f"single-threaded C pinned to one core, {el:.1f} s")}
+    if alg_bytes_per_token > 0:   # the same algorithmic bytes per token as the GPU line
+        out["gbs"] = round(done / el * alg_bytes_per_token / 1e9, 3)
+    return out
 
 
 # ---------------------------------------------------------------- main
@@ -844,7 +855,15 @@ def run_ours(args, rank, world, local_rank):
     line = assemble_line(args, world, head, results, clocks, peak, peak_kind)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(results[head][0])
+            def per_token(r, wo):
+                return (r["dispatch_alg_bytes"] + r["combine_alg_bytes"]) / wo.T
+            wh, _, rh = results[head]
+            line["cpu_baseline"] = cpu_baseline(wh, alg_bytes_per_token=per_token(rh, wh))
+            # every other workload's oracle, once each on a shorter sample
+            for name, (wo, _, r) in results.items():
+                if name != head:
+                    line["workloads"][name]["cpu_baseline"] = cpu_baseline(
+                        wo, budget_s=3.0, alg_bytes_per_token=per_token(r, wo))
         print(json.dumps(line), flush=True)
     return 0
 
