@@ -494,7 +494,8 @@ def measure_e2e(runner, steps, world, flush):
     * pipelined (the reported throughput): uploads on one copy stream,
       dispatch + combine (output in HBM) on the compute stream, downloads on
       a second copy stream, inputs and outputs double-buffered, so step s+1's
-      upload and step s-1's download run while step s computes.  Every step
+      upload (queued before step s's own calls) and step s-1's download run
+      while step s computes.  Every step
       still moves its own inputs and result across the link.  The K steps
       are captured once as one CUDA graph and replayed (issuing the copies,
       event waits and two API calls of a step from Python takes longer than
@@ -540,18 +541,27 @@ def measure_e2e(runner, steps, world, flush):
     out_free = [torch.cuda.Event() for _ in range(2)]
     saved = (runner.x, runner.idx, runner.wts, runner.out)
 
+    def upload(s):
+        j = s % 2
+        with torch.cuda.stream(s_in):
+            if s >= 2:
+                s_in.wait_event(in_free[j])         # step s-2 has read this input slot
+            xs[j].copy_(hx, non_blocking=True)
+            ids[j].copy_(hi, non_blocking=True)
+            wts[j].copy_(hw, non_blocking=True)
+            in_ready[j].record(s_in)
+
     def run(n, comp):
         s_in.wait_stream(comp)
         s_out.wait_stream(comp)
+        upload(0)
         for s in range(n):
             j = s % 2
-            with torch.cuda.stream(s_in):
-                if s >= 2:
-                    s_in.wait_event(in_free[j])     # step s-2 has read this input slot
-                xs[j].copy_(hx, non_blocking=True)
-                ids[j].copy_(hi, non_blocking=True)
-                wts[j].copy_(hw, non_blocking=True)
-                in_ready[j].record(s_in)
+            # the next step's upload is queued before this step's API calls:
+            # a step that waits on the host for its receive counts then no
+            # longer holds the upload stream back while the host wakes up
+            if s + 1 < n:
+                upload(s + 1)
             comp.wait_event(in_ready[j])
             if s >= 2:
                 comp.wait_event(out_free[j])        # step s-2's output has left this slot
