@@ -53,7 +53,7 @@ namespace ep {
 // One warp's TMA pipeline over a sequence of units; unit u is piece u % P of
 // token u / P.  The sequence (UnitSeq below) starts with kSeqStatic units
 // first + j * stride, and continues either the same way or, with a
-// workspace counter, with units claimed one at a time as the warp goes: SMs
+// workspace counter, with units claimed in batches as the warp goes: SMs
 // of a GB300 do not all stream at the same rate (a static split of the
 // 152 SMs' work measured CTAs finishing between 0.62x and 1.0x of the
 // slowest one's time), so a warp on a faster SM takes more units.
