@@ -2,12 +2,9 @@
 dispatch casts, fp32 -> bf16 as the combine rounds) against the oracle's
 encoders, written from the OCP FP8 and bfloat16 definitions.
 
-E4M3: every fp32 bit pattern whose exponent can round to a non-zero finite
-E4M3 value or to the saturation boundary (2^-12 <= |x| < 2^10, both signs,
-all 2^23 mantissas: 369 M inputs), all fp32 subnormals, and a random sample
-elsewhere.  bf16: all 2^16 low halves under every sign and exponent with the
-kept mantissa at its edges (0, 1, 0x3F, 0x40, 0x7E, 0x7F; 201 M inputs), and a
-random sample.  NaN inputs must give a NaN; everything else bit for bit."""
+Both conversions are checked on every one of the 2^32 fp32 bit patterns
+(in chunks of 2^26, the oracle's encoder run over host threads).  NaN
+inputs must give a NaN; everything else bit for bit."""
 import concurrent.futures as cf
 import os
 
@@ -66,37 +63,22 @@ def _check_bf16(bits: torch.Tensor):
                            f"{hex(int(xh[bad][:1].view(np.uint32)[0]))}")
 
 
-def test_e4m3_every_input_near_its_range():
-    man = torch.arange(1 << 23, dtype=torch.int64, device="cuda")
-    for exp in range(127 - 12, 127 + 10):
-        for sign in (0, 1):
-            _check_e4m3((sign << 31) | (exp << 23) | man)
+_CHUNK = 1 << 26
 
 
-def test_e4m3_subnormals_specials_and_a_sample():
-    man = torch.arange(1 << 23, dtype=torch.int64, device="cuda")
-    _check_e4m3(torch.cat([man, (1 << 31) | man]))                    # fp32 subnormals, zeros
-    nan_inf = torch.cat([(255 << 23) | man[:1 << 16], (1 << 31) | (255 << 23) | man[:1 << 16]])
-    _check_e4m3(nan_inf)                                              # inf and NaNs
-    g = torch.Generator(device="cuda")
-    g.manual_seed(11)
-    _check_e4m3(torch.randint(0, 1 << 32, (1 << 24,), generator=g, device="cuda",
-                              dtype=torch.int64))
+@pytest.mark.slow
+def test_e4m3_every_fp32_bit_pattern():
+    """All 2^32 inputs: zeros, subnormals, every exponent and mantissa of
+    both signs, infinities and NaNs."""
+    for start in range(0, 1 << 32, _CHUNK):
+        _check_e4m3(torch.arange(start, start + _CHUNK, dtype=torch.int64, device="cuda"))
 
 
-def test_bf16_every_low_half_at_the_mantissa_edges():
-    low = torch.arange(1 << 16, dtype=torch.int64, device="cuda")
-    for m7 in (0x00, 0x01, 0x3F, 0x40, 0x7E, 0x7F):
-        hi = torch.tensor([(s << 15) | (e << 7) | m7 for s in (0, 1) for e in range(256)],
-                          dtype=torch.int64, device="cuda")
-        _check_bf16(((hi[:, None] << 16) | low[None, :]).reshape(-1))
-
-
-def test_bf16_random_sample():
-    g = torch.Generator(device="cuda")
-    g.manual_seed(12)
-    _check_bf16(torch.randint(0, 1 << 32, (1 << 24,), generator=g, device="cuda",
-                              dtype=torch.int64))
+@pytest.mark.slow
+def test_bf16_every_fp32_bit_pattern():
+    """All 2^32 inputs, each rounded to nearest even on its low 16 bits."""
+    for start in range(0, 1 << 32, _CHUNK):
+        _check_bf16(torch.arange(start, start + _CHUNK, dtype=torch.int64, device="cuda"))
 
 
 def test_format_entry_points_reject_odd_lengths():
