@@ -25,6 +25,7 @@ value = total tokens / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -343,6 +344,24 @@ def workload_desc(w) -> str:
             f"top-{w.k}, {fp8[w.fp8_mode]} {mode} dispatch + bf16 combine{extra}")
 
 
+class no_gc:
+    """Python's garbage collector off for a timed loop: a collection in the
+    middle of it stalls the host for milliseconds, and a step that waits on
+    the host for its receive counts then takes the stall on the GPU clock.
+    (No collection before it: a full collection made the host-waiting steps
+    ~20 us slower, the freed memory being faulted back in by the loop.)"""
+
+    def __enter__(self):
+        self.was = gc.isenabled()
+        gc.disable()
+        return self
+
+    def __exit__(self, *exc):
+        if self.was:
+            gc.enable()
+        return False
+
+
 def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
     import torch
 
@@ -360,14 +379,15 @@ def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
     barrier(world, runner.dev)
     torch.cuda.synchronize()
     launches0 = ep.ep_launch_count()
-    t_wall = time.perf_counter()
-    for s in range(steps):
-        flush.fill_(s & 0xFF)
-        outer[s][0].record()
-        runner.step()
-        outer[s][1].record()
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t_wall
+    with no_gc():
+        t_wall = time.perf_counter()
+        for s in range(steps):
+            flush.fill_(s & 0xFF)
+            outer[s][0].record()
+            runner.step()
+            outer[s][1].record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
     barrier(world, runner.dev)
     launches = ep.ep_launch_count() - launches0
     step_ms = [a.elapsed_time(b) for a, b in outer]
@@ -376,11 +396,12 @@ def measure(runner, steps: int, warmup: int, world: int, flush, e2e: bool):
     # enqueues the step without the host wait for the receive counts)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     torch.cuda.synchronize()
-    for s in range(steps):
-        flush.fill_(s & 0xFF)
-        evs[s][4].record()   # step start: layout + notify run before e[0] in normal mode
-        runner.step(evs[s][:4])
-    torch.cuda.synchronize()
+    with no_gc():
+        for s in range(steps):
+            flush.fill_(s & 0xFF)
+            evs[s][4].record()   # step start: layout + notify run before e[0] in normal mode
+            runner.step(evs[s][:4])
+        torch.cuda.synchronize()
     disp_ms = [e[0].elapsed_time(e[1]) for e in evs]
     comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
     ln_ms = [e[4].elapsed_time(e[0]) for e in evs]
@@ -517,15 +538,16 @@ def measure_e2e(runner, steps, world, flush):
     try:
         barrier(world, runner.dev)
         torch.cuda.synchronize()
-        for s in range(steps):
-            flush.fill_(s & 0xFF)
-            evs[s][0].record()
-            runner.x.copy_(hx, non_blocking=True)
-            runner.idx.copy_(hi, non_blocking=True)
-            runner.wts.copy_(hw, non_blocking=True)
-            runner.step()
-            evs[s][1].record()
-        torch.cuda.synchronize()
+        with no_gc():
+            for s in range(steps):
+                flush.fill_(s & 0xFF)
+                evs[s][0].record()
+                runner.x.copy_(hx, non_blocking=True)
+                runner.idx.copy_(hi, non_blocking=True)
+                runner.wts.copy_(hw, non_blocking=True)
+                runner.step()
+                evs[s][1].record()
+            torch.cuda.synchronize()
     finally:
         runner.out = dev_out
     serial_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
@@ -591,13 +613,14 @@ def measure_e2e(runner, steps, world, flush):
             torch.cuda.synchronize()
         barrier(world, runner.dev)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(comp)
-        if graph is not None:
-            graph.replay()
-        else:
-            run(steps, comp)
-        t1.record(comp)
-        torch.cuda.synchronize()
+        with no_gc():
+            t0.record(comp)
+            if graph is not None:
+                graph.replay()
+            else:
+                run(steps, comp)
+            t1.record(comp)
+            torch.cuda.synchronize()
         del graph
     finally:
         runner.x, runner.idx, runner.wts, runner.out = saved
