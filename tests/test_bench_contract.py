@@ -93,3 +93,22 @@ def test_gpu_arm_line_from_measurements():
     rd = wd["roofline"]
     assert rd["kernel"] == "k_combine" and rd["frac"] == pytest.approx(
         results["decode"][2]["combine_gbs"] / 6750.0, abs=1e-3)
+
+
+def test_traffic_key_ignores_comments_but_not_code(tmp_path):
+    """The DRAM traffic the bench reports is keyed to a hash of the kernel
+    source's code: a comment or whitespace edit keeps the key, a code edit
+    changes it (and voids the stored traffic)."""
+    import bench
+    base = "// a kernel\n__global__ void k(int* p) {\n  p[0] = 1;   /* store */\n}\n"
+    variants = {
+        "comment": "// the same kernel, described differently\n__global__ void k(int* p) {\n  p[0] = 1;   /* one store */\n}\n",
+        "spacing": "__global__   void k(int* p)\n{\n    p[0] = 1;\n}\n",
+        "code": "// a kernel\n__global__ void k(int* p) {\n  p[0] = 2;   /* store */\n}\n",
+    }
+    src = tmp_path / "k.cu"
+    src.write_text(base)
+    key = bench.kernel_hash(str(src))
+    for name, text in variants.items():
+        src.write_text(text)
+        assert (bench.kernel_hash(str(src)) == key) == (name != "code"), name
