@@ -666,14 +666,16 @@ int launch_scale_columns(const ScaleColParams& p, bool ll, int fp8_mode, cudaStr
 // Small FP8 batches: pieces shrink (to kMinFp8Piece channels at the least)
 // until every warp of the launch has about kMinUnitsPerWarp units.  The
 // skewed workload (8192 tokens, H = 4096) gets 6.7 units per warp with the
-// 2048-channel pieces that fit, 13.5 with 1024-channel ones; measured in the
-// timed step (L2 dirty after the flush), the scatter alone takes 52.2 us
-// instead of 53.3 and the column pass behind it 6.7 instead of 8.1, the
-// dispatch 58.9 instead of 61.4 (768-channel pieces were slower again).
-// Cold and serialised under ncu the scatter alone is the slower one (55 us
-// against 49): the gain is in the conditions of the step.
+// 2048-channel pieces that fit; measured in the timed step (L2 dirty after
+// the flush): 1024-channel pieces (13.5 units per warp) made its dispatch
+// 58.9 us instead of 61.4 (the scatter alone 52.2 instead of 53.3, the
+// column pass behind it 6.7 instead of 8.1), 1408-channel ones (3 pieces,
+// 10.1 units per warp: this rule) 57.5-58.0 against 59.2-59.5 for 1024 on
+// another box, 768-channel ones were slower again.  Cold and serialised
+// under ncu the smaller pieces are the slower ones: the gain is in the
+// conditions of the step.
 constexpr int kMinFp8Piece = 1024;
-constexpr int kMinUnitsPerWarp = 16;
+constexpr int kMinUnitsPerWarp = 10;
 
 // Piece size, per-warp shared memory and warps per CTA: the largest piece
 // (a multiple of the 16-byte / 128-channel granule) whose stages fit the
