@@ -676,11 +676,17 @@ int launch_scale_columns(const ScaleColParams& p, bool ll, int fp8_mode, cudaStr
 // conditions of the step.
 constexpr int kMinFp8Piece = 1024;
 constexpr int kMinUnitsPerWarp = 10;
+// Every other batch: pieces of at most kMaxPiece channels (1 KB E4M3 or 2 KB
+// bf16 rows per bulk store): large dispatch 1464-1466 us against 1480-1483
+// with the 1792-channel pieces that fit, prefill 644-646 against 653-655;
+// 768-channel pieces were slower than either (interleaved A/B, three runs).
+constexpr int kMaxPiece = 1024;
 
 // Piece size, per-warp shared memory and warps per CTA: the largest piece
 // (a multiple of the 16-byte / 128-channel granule) whose stages fit the
-// per-warp share of `budget` for `target_warps` warps (FP8: smaller for a
-// small batch, above).
+// per-warp share of `budget` for `target_warps` warps, then shrunk by the
+// rules above (a small FP8 batch toward kMinUnitsPerWarp units per warp,
+// any other batch to kMaxPiece channels).
 static void plan_pipeline(ScatterParams& p, int fp8_mode, int target_warps, size_t budget) {
   const bool fp8 = fp8_mode != EP_FP8_NONE;
   const int gran = fp8 ? kFp8Block : 8;
@@ -699,11 +705,16 @@ static void plan_pipeline(ScatterParams& p, int fp8_mode, int target_warps, size
     ++P;
     hp = ((p.H + P - 1) / P + gran - 1) / gran * gran;
   }
-  if (fp8) {
-    const int64_t warps = (int64_t)ep_host::grid_cap(1) * target_warps;
+  const int64_t warps = (int64_t)ep_host::grid_cap(1) * target_warps;
+  if (fp8 && p.T * (int64_t)P < kMinUnitsPerWarp * warps) {
     while (hp > kMinFp8Piece && p.T * (int64_t)P < kMinUnitsPerWarp * warps) {
       ++P;
       hp = std::max(kMinFp8Piece, ((p.H + P - 1) / P + gran - 1) / gran * gran);
+    }
+  } else {
+    while (hp > kMaxPiece) {
+      ++P;
+      hp = ((p.H + P - 1) / P + gran - 1) / gran * gran;
     }
   }
   P = (p.H + hp - 1) / hp;
