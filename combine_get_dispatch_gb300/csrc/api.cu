@@ -32,6 +32,26 @@ int num_sms() {
   return cached[dev];
 }
 
+int64_t l2_bytes() {
+  static std::mutex mu;
+  static int64_t cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 1;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 static std::atomic<int> g_sm_budget{0};   // 0: every SM
 
 int grid_cap(int ctas_per_sm) {

@@ -17,9 +17,13 @@
 //
 // One warp handles one (token, 512-channel segment) item: every lane issues
 // all k row loads of its 2 x 16 bytes before the first fma (k*2 independent
-// 16-byte streaming loads in flight per lane, marked evict-first in L2: each
-// row is read once, and the dispatch's output may still be in L2), then
-// reduces in registers and stores 2 x 16 bytes of bf16.  Rows are read whole
+// 16-byte streaming loads in flight per lane), then reduces in registers and
+// stores 2 x 16 bytes of bf16.  The row loads carry an L2 evict-first hint
+// (each row is read once, and the dispatch's rows still dirty in L2 are then
+// not the lines evicted) unless the combine reads many times the L2
+// (kNoHintL2Multiple): decode combine 49.1-49.4 us with the hint against
+// 52.3-52.9 without, skewed 81.4-81.7 against 85.1-86.0, but the large
+// combine (15 GB of rows) 2.462-2.466 ms with it against 2.408-2.435 without.  Rows are read whole
 // and in order, so every warp load instruction moves 512 contiguous bytes.
 
 #include "ep_common.cuh"
@@ -40,7 +44,9 @@ struct CombineParams {
   int32_t* status;
 };
 
-template <int kU, int kK>
+constexpr int64_t kNoHintL2Multiple = 32;   // rows read beyond this many L2 sizes: no hint
+
+template <int kU, int kK, bool kHint>
 __global__ void __launch_bounds__(2 * kCombineThreads, 1) k_combine(CombineParams p) {
   constexpr int kSegC = kU * kWarp * 8;
   // launched as a programmatic dependent: the CTAs may be resident before
@@ -82,7 +88,8 @@ __global__ void __launch_bounds__(2 * kCombineThreads, 1) k_combine(CombineParam
 #pragma unroll
       for (int j = 0; j < kK; ++j) {
         if (j < p.k && f[j] >= 0 && ch < p.H)
-          v[u][j] = ld_stream_v4(p.y + (int64_t)f[j] * row_bytes + (int64_t)ch * 2, pol);
+          v[u][j] = kHint ? ld_stream_v4(p.y + (int64_t)f[j] * row_bytes + (int64_t)ch * 2, pol)
+                          : __ldg(reinterpret_cast<const uint4*>(p.y + (int64_t)f[j] * row_bytes + (int64_t)ch * 2));
         else
           v[u][j] = make_uint4(0, 0, 0, 0);
       }
@@ -119,7 +126,7 @@ __global__ void __launch_bounds__(2 * kCombineThreads, 1) k_combine(CombineParam
   }
 }
 
-template <int kU, int kK>
+template <int kU, int kK, bool kHint>
 static int launch_combine_t(const CombineParams& p, cudaStream_t stream) {
   constexpr int kSegC = kU * kWarp * 8;
   CombineParams q = p;
@@ -141,7 +148,7 @@ static int launch_combine_t(const CombineParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, k_combine<kU, kK>, q) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, k_combine<kU, kK, kHint>, q) != cudaSuccess) {
     cudaGetLastError();
     return EP_ERR_CUDA;
   }
@@ -150,8 +157,11 @@ static int launch_combine_t(const CombineParams& p, cudaStream_t stream) {
 }
 
 static int launch_combine(const CombineParams& p, cudaStream_t stream) {
-  if (p.k <= 8) return launch_combine_t<2, 8>(p, stream);
-  return launch_combine_t<1, 16>(p, stream);
+  // rows read at most: every slot of every token, H bf16 channels each
+  const bool hint = p.T * p.k * (int64_t)p.H * 2 <= kNoHintL2Multiple * ep_host::l2_bytes();
+  if (p.k <= 8)
+    return hint ? launch_combine_t<2, 8, true>(p, stream) : launch_combine_t<2, 8, false>(p, stream);
+  return hint ? launch_combine_t<1, 16, true>(p, stream) : launch_combine_t<1, 16, false>(p, stream);
 }
 
 static int check_combine(const void* y, const float* w, const int32_t* cidx, int R, int T_r, int H,

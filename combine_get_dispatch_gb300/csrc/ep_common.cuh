@@ -302,6 +302,7 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 // Host-side helpers shared by the entry points (defined in api.cu).
 namespace ep_host {
 int num_sms();   // SMs of the current device
+int64_t l2_bytes();   // L2 cache size of the current device
 // Upper bound on a data kernel's grid: ctas_per_sm CTAs on every SM, or,
 // while an SM budget is set (ep_set_num_sms), one CTA on each of that many.
 int grid_cap(int ctas_per_sm);
