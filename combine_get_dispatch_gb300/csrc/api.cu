@@ -2,8 +2,8 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
 #include <mutex>
-#include <set>
 #include <utility>
 
 #include "ep_common.cuh"
@@ -97,14 +97,15 @@ int ensure_max_smem(const void* func, int bytes) {
     return EP_ERR_CUDA;
   }
   static std::mutex mu;
-  static std::set<std::pair<const void*, int>> done;
+  static std::map<std::pair<const void*, int>, int> done;   // largest limit set per (kernel, device)
   std::lock_guard<std::mutex> lock(mu);
-  if (done.count({func, dev})) return EP_OK;
+  const auto it = done.find({func, dev});
+  if (it != done.end() && it->second >= bytes) return EP_OK;
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
     cudaGetLastError();
     return EP_ERR_CUDA;
   }
-  done.insert({func, dev});
+  done[{func, dev}] = bytes;
   return EP_OK;
 }
 

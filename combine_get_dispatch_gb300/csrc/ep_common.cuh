@@ -314,8 +314,9 @@ bool sm_budget_set();
 int device_view(void* p, void** dev);
 void count_launch(int n = 1);
 int check_launch();   // EP_OK or EP_ERR_CUDA after a launch
-// Opt a kernel into `bytes` of dynamic shared memory on the current device
-// (once per kernel and device: the attribute is per device).
+// Opt a kernel into at least `bytes` of dynamic shared memory on the current
+// device (the attribute is per device; it is set again only when a call asks
+// for more than the largest limit set so far for that kernel and device).
 int ensure_max_smem(const void* func, int bytes);
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace ep_host
