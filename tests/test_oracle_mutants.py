@@ -32,6 +32,10 @@ MUTANTS = {
                             "? ldexp(1.0, -10) : ldexp(1.0, ilogb(a) - 3)", 0),
     # FP8 block quantisation
     "amax_floor_dropped": ("if (amax < 1e-4f) amax = 1e-4f;", "if (amax <= 0.0f) amax = 1e-30f;", 0),
+    "amax_over_half_the_block": ("    for (int c = 0; c < BLOCK_CHANNELS; ++c) {\n      float a = fabsf(",
+                                 "    for (int c = 0; c < BLOCK_CHANNELS / 2; ++c) {\n      float a = fabsf(", 0),
+    "ue8m0_byte_one_low": ("scale_ue8m0[(int64_t)b * scale_stride] = (uint8_t)biased;",
+                           "scale_ue8m0[(int64_t)b * scale_stride] = (uint8_t)(biased - 1u);", 0),
     "amax_infinity_not_capped": ("if (amax > FLT_MAX) amax = FLT_MAX;", "", 0),
     "fp32_scale_inverted": ("float scale = amax / 448.0f;", "float scale = 448.0f / amax;", 0),
     "fp32_max_240": ("float inv = 448.0f / amax;", "float inv = 240.0f / amax;", 0),
@@ -58,6 +62,9 @@ MUTANTS = {
                                 "      run += num_tokens_per_expert[(int64_t)i * E + e];\n"
                                 "      expert_prefix[(int64_t)i * E + e] = run;", 0),
     "alignment_rounds_down": ("((run + a - 1) / a) * a", "(run / a) * a", 0),
+    "expert_totals_row_dropped": ("    expert_prefix[(int64_t)R * E + e] = run;\n", "", 0),
+    "psum_shifted_by_one": ("psum[(int64_t)r * (E_l + 1) + l + 1] = s;",
+                            "psum[(int64_t)r * (E_l + 1) + l] = s;", 0),
     "psum_wrong_rank": ("s += num_recv_tokens_per_expert[(int64_t)r * E_l + l];",
                         "s += num_recv_tokens_per_expert[(int64_t)l];", 0),
     "worst_tokens_off_by_one": ("run > num_worst_tokens", "run >= num_worst_tokens", 0),
@@ -70,6 +77,10 @@ MUTANTS = {
         "psum[(int64_t)r * (E_l + 1) + l] + slot_rank[p];", 0),
     "dispatch_local_index_transposed": ("int l = (int)(e % E_l);", "int l = (int)(e / R);", 0),
     "dispatch_src_idx_local": ("recv_src_idx[flat] = i * T_r + t;", "recv_src_idx[flat] = t;", 0),
+    "dispatch_combine_idx_without_rank": ("combine_idx[p] = (int32_t)flat;",
+                                          "combine_idx[p] = (int32_t)row;", 0),
+    "dispatch_scales_without_rank": ("(int64_t)r * nb * cap_rows + row, cap_rows);",
+                                     "row, cap_rows);", 0),
     "dispatch_capacity_not_reported": (
         "          combine_idx[p] = -1;\n          rc = ORACLE_ERR_CAPACITY;\n          continue;",
         "          combine_idx[p] = -1;\n          continue;", 0),
@@ -83,8 +94,16 @@ MUTANTS = {
                                     "if (R <= 0 || E % R != 0 ||", 0),
     "ll_row_drops_source_offset": ("int64_t row = (int64_t)eprefix[(int64_t)i * E + e] + slot_rank[p];",
                                    "int64_t row = (int64_t)slot_rank[p];", 0),
+    "ll_src_info_local": ("packed_recv_src_info[flat] = i * T_r + t;",
+                          "packed_recv_src_info[flat] = t;", 0),
+    "ll_combine_idx_without_expert": ("combine_idx[p] = (int32_t)flat;",
+                                      "combine_idx[p] = (int32_t)row;", 1),
+    "ll_scales_row_major": ("e * nb * seg_rows + row, seg_rows);",
+                            "(e * seg_rows + row) * nb, 1);", 0),
     # combine
     "combine_weight_of_slot0": ("acc = fmaf(topk_weights[t * k + j],", "acc = fmaf(topk_weights[t * k],", 0),
+    "combine_starts_from_minus_zero": ("      float acc = 0.0f;\n      for (int j = 0; j < k; ++j) {\n        int32_t f = combine_idx[t * k + j];\n        if (f < 0) continue;\n        acc = fmaf(",
+                                       "      float acc = -0.0f;\n      for (int j = 0; j < k; ++j) {\n        int32_t f = combine_idx[t * k + j];\n        if (f < 0) continue;\n        acc = fmaf(", 0),
     "combine_weight_dropped": ("acc = fmaf(topk_weights[t * k + j], ep_oracle_bf16_to_f32(y[(int64_t)f * H + h]), acc);",
                                "acc = acc + ep_oracle_bf16_to_f32(y[(int64_t)f * H + h]);", 0),
     # once-per-rank layout and combine
@@ -94,6 +113,9 @@ MUTANTS = {
         "          combine_idx[base + first] = -1;", 0),
     "rank_topk_global_index": ("recv_topk_idx[flat * k + j] = on_r ? e - (int64_t)r * E_l : -1;",
                                "recv_topk_idx[flat * k + j] = on_r ? e : -1;", 0),
+    "rank_first_slot_is_last": ("            first = j;\n            break;", "            first = j;", 0),
+    "rank_src_idx_local": ("recv_src_idx[flat] = i * T_r + t;", "recv_src_idx[flat] = t;", 1),
+    "rank_topk_weight_dropped": ("on_r ? topk_weights[base + j] : 0.0f;", "on_r ? 1.0f : 0.0f;", 0),
     "rank_combine_keeps_last": ("acc = acc + ep_oracle_bf16_to_f32(y[(int64_t)f * H + h]);",
                                 "acc = ep_oracle_bf16_to_f32(y[(int64_t)f * H + h]);", 0),
 }
