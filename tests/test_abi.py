@@ -124,3 +124,12 @@ def test_binding_rejects_host_tensors():
     idx = torch.zeros((2, 4, 2), dtype=torch.int64)
     with pytest.raises(ValueError):
         ep.ep_get_dispatch_layout(idx, 4, *[torch.zeros(1)] * 4, torch.zeros(1, dtype=torch.uint8))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No CPU or PyTorch fallback: without the built library the binding
+    raises instead of computing anything."""
+    monkeypatch.setattr(ep, "_lib", None)
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "libep.so"))
+    with pytest.raises(RuntimeError, match="libep.so not found"):
+        ep.load(build_if_missing=False)
