@@ -59,18 +59,6 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v
   return old;
 }
 
-// atomicAdd with release semantics at GPU scope (the arrival at a barrier
-// whose waiters then read with acquire loads).
-__device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -168,10 +156,6 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
-}
-
-__device__ __forceinline__ void st_v2(void* p, uint2 v) {
-  asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA bulk copies / mbarrier
