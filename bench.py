@@ -74,8 +74,6 @@ def parse_args(argv=None):
     # profiling aids (change the workload; never used for a reported number)
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override T_r of every selected workload (profiling only)")
-    ap.add_argument("--no-combine", action="store_true",
-                    help="dispatch only, no expert-output buffer (profiling only)")
     ap.add_argument("--separate-layout-notify", action="store_true",
                     help="normal mode: ep_get_dispatch_layout + ep_notify_dispatch as two "
                          "launches instead of ep_layout_notify (comparison)")
@@ -193,7 +191,7 @@ def alg_bytes(w, rows: int):
 class Runner:
     """Buffers and one step of one workload on the current GPU."""
 
-    def __init__(self, w, device, with_combine=True, fused_layout_notify=True):
+    def __init__(self, w, device, fused_layout_notify=True):
         import numpy as np
         import torch
 
@@ -210,15 +208,13 @@ class Runner:
         self.rows = int((idx >= 0).sum())
         self.ll = w.mode == "ll"
         self.rank = w.mode == "rank"
-        self.with_combine = with_combine
         # a step without a host wait can be captured in a CUDA graph
         self.capturable = self.ll or w.num_worst_tokens >= 0
         if self.ll:
             self.buf = ep.alloc_ll(w.R, w.T_r, w.H, w.E, w.k, w.max_tokens_per_rank, w.fp8_mode,
                                    device=device)
             S = w.R * w.max_tokens_per_rank
-            if with_combine:
-                self.y = synth.expert_outputs_torch(w.E * S, w.H, device).view(w.R, w.E_l, S, w.H)
+            self.y = synth.expert_outputs_torch(w.E * S, w.H, device).view(w.R, w.E_l, S, w.H)
         elif self.rank:   # once per (token, destination rank): experts' = ranks
             E_l = w.E // w.R
             r_of = np.where(idx >= 0, idx // E_l, -1)
@@ -232,9 +228,8 @@ class Runner:
             self.buf = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, self.cap, device=device)
             self.rtk = torch.empty((w.R, self.cap, w.k), dtype=torch.int64, device=device)
             self.rtw = torch.empty((w.R, self.cap, w.k), dtype=torch.float32, device=device)
-            if with_combine:
-                self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(
-                    w.R, self.cap, w.H)
+            self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(
+                w.R, self.cap, w.H)
         else:
             self.lay = ep.alloc_layout(w.R, w.T_r, w.k, w.E, device=device)
             self.nt = ep.alloc_notify(w.R, w.E, device=device)
@@ -245,9 +240,8 @@ class Runner:
                 self._layout_notify()   # padded to a multiple of 16 rows
                 self.cap = (int(self.host_rows.max()) + 15) // 16 * 16
             self.buf = ep.alloc_dispatch(w.R, w.T_r, w.H, w.k, w.fp8_mode, self.cap, device=device)
-            if with_combine:
-                self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(
-                    w.R, self.cap, w.H)
+            self.y = synth.expert_outputs_torch(w.R * self.cap, w.H, device).view(
+                w.R, self.cap, w.H)
         torch.cuda.synchronize()
 
     def _layout_notify(self, host_wait=True):
@@ -276,8 +270,7 @@ class Runner:
         ep.ep_layout_notify_dispatch(self.x, self.idx, w.E, w.fp8_mode, w.expert_alignment,
                                      w.num_worst_tokens, self.cap, self.lay, self.nt, b, self.ws,
                                      self.status)
-        if self.with_combine:
-            ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
+        ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
 
     def step(self, ev=None):
         """One pass; ev = (e0, e1, e2, e3) events around dispatch / combine.
@@ -296,9 +289,8 @@ class Runner:
             if ev:
                 ev[1].record()
                 ev[2].record()
-            if self.with_combine:
-                ep.ep_ll_combine(self.y, self.wts, b["combine_idx"], w.E, w.max_tokens_per_rank,
-                                 self.out, self.status)
+            ep.ep_ll_combine(self.y, self.wts, b["combine_idx"], w.E, w.max_tokens_per_rank,
+                             self.out, self.status)
             if ev:
                 ev[3].record()
         elif self.rank:
@@ -314,8 +306,7 @@ class Runner:
             if ev:
                 ev[1].record()
                 ev[2].record()
-            if self.with_combine:
-                ep.ep_rank_combine(self.y, b["combine_idx"], self.cap, self.out, self.status)
+            ep.ep_rank_combine(self.y, b["combine_idx"], self.cap, self.out, self.status)
             if ev:
                 ev[3].record()
         else:
@@ -329,8 +320,7 @@ class Runner:
             if ev:
                 ev[1].record()
                 ev[2].record()
-            if self.with_combine:
-                ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
+            ep.ep_combine(self.y, self.wts, b["combine_idx"], self.cap, self.out, self.status)
             if ev:
                 ev[3].record()
 
@@ -870,13 +860,12 @@ def run_ours(args, rank, world, local_rank):
     clocks = None
     for name in names:
         w = workload(name, args.tokens_per_rank)
-        runner = Runner(w, dev, with_combine=not args.no_combine,
-                        fused_layout_notify=not args.separate_layout_notify)
+        runner = Runner(w, dev, fused_layout_notify=not args.separate_layout_notify)
         sampler = ClockSampler(local_rank) if name == head else None
         if sampler:
             sampler.start()
         res = measure(runner, args.steps, args.warmup, world, flush,
-                      e2e=(name == head and not args.no_e2e and not args.no_combine))
+                      e2e=(name == head and not args.no_e2e))
         if sampler:
             clocks = sampler.stop()
         res["step_ms_max"] = max_over_ranks(res["step_ms"], world)
@@ -887,7 +876,7 @@ def run_ours(args, rank, world, local_rank):
         res["tokens"] = w.T
         if name == head or name == "skewed":
             res["launch_latency_us"] = measure_launch_latency(runner, args.steps, flush)
-        if not runner.ll and not runner.rank and w.num_worst_tokens >= 0 and not args.no_combine:
+        if not runner.ll and not runner.rank and w.num_worst_tokens >= 0:
             res["single_call"] = measure_single_call(runner, args.steps, flush)
         results[name] = (w, runner, res)
         if name != head:
@@ -919,15 +908,13 @@ def config_of(w, world: int) -> dict:
                            + " dispatch; y bf16 -> bf16 combine, fp32 accumulate")}
 
 
-def roofline_of(name, w, runner, res, peak, peak_kind, dispatch_only=False):
+def roofline_of(name, w, runner, res, peak, peak_kind):
     """Roofline object of a workload's dominant kernel (the longer of its
     dispatch and combine): algorithmic bytes per launch over the CUDA-event
     time of the launch, against the HBM copy peak; traffic = DRAM bytes per
     launch from the committed ncu summary while the kernel source is
     unchanged since it was taken, else null."""
     dom = "combine" if res["combine_ms"] >= res["dispatch_ms"] else "dispatch"
-    if dispatch_only:
-        dom = "dispatch"
     kern = {"combine": "k_combine", "dispatch": "k_ll_fused" if runner.ll else "k_scatter"}[dom]
     src = os.path.join(ROOT, "combine_get_dispatch_gb300", "csrc",
                        "combine.cu" if dom == "combine"
@@ -966,7 +953,7 @@ def assemble_line(args, world, head, results, clocks, peak, peak_kind):
                         "dispatch_frac": round(res["dispatch_gbs"] / peak, 4),
                         "combine_frac": round(res["combine_gbs"] / peak, 4)},
             "clocks": clocks, "e2e": e2e, "gpu_launches": res["launches"],
-            "roofline": roofline_of(head, w, runner, res, peak, peak_kind, args.no_combine)}
+            "roofline": roofline_of(head, w, runner, res, peak, peak_kind)}
     if "wall_s" in res:
         line["timed_region_s"] = round(res["wall_s"], 4)
     others = {}
@@ -982,7 +969,7 @@ def assemble_line(args, world, head, results, clocks, peak, peak_kind):
             "combine_frac": round(r["combine_gbs"] / peak, 4),
             "layout_notify_ms": round(r.get("layout_notify_ms", 0.0), 4),
             "gpu_launches": r["launches"],
-            "roofline": roofline_of(name, wo, ro, r, peak, peak_kind, args.no_combine)}
+            "roofline": roofline_of(name, wo, ro, r, peak, peak_kind)}
         if r.get("launch_latency_us"):
             others[name]["launch_latency_us"] = r["launch_latency_us"]
         if r.get("single_call"):
